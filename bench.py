@@ -1,0 +1,396 @@
+"""Benchmark of one MoE prefill layer (quantize-scatter -> group gather -> grouped
+MMQ gate/up -> hidden re-quantization -> grouped MMQ down -> top-k combine) on
+GB300, through the library's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Prints one JSON line.  A step is one whole layer over the T=8192 workload
+(d=2048, f=768, E=512, K=10, Q8_0 weights, Zipf-skewed routing) by default.
+Inputs are resident in HBM when the timed region starts; L2 is flushed by a
+512 MB write between steps (outside the per-step CUDA events).  Per-stage CUDA
+events give the phase table, the quantizer GB/s and the dominant kernel's
+roofline.  ``e2e`` repeats the measurement with the step's inputs copied from
+pinned host memory and the output read back inside the timed region.
+``--impl reference`` times the CPU oracle (single thread, host cores) on a
+bounded token sample of the same workload instead.
+Under torchrun each rank runs its own replica (weak scaling, no collective on
+the data path); the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_workloads as mw  # noqa: E402
+
+METRIC = "MoE prefill layer tokens/s at T=8192 (1 GB300) + % roofline; quantize GB/s"
+DEFAULT_CONFIG = mw.T8192.name
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ bytes / ops --
+
+def layer_accounting(cfg, n_active: int, rec_bytes: int, R: int):
+    T, d, f, K = cfg.T, cfg.d, cfg.f, cfg.K
+    q8 = 1.125  # bytes per q8_1 value: int8 plus (d, s) fp16 per 32
+    stages = {
+        "slot_map": ("hbm", T * K * 4 * 4),
+        "quantize_scatter": ("hbm", T * d * 4 + R * d * q8 + T * K * 4),
+        "group_gather": ("hbm", 2 * n_active * rec_bytes),
+        "mmq_gateup": ("tensor", 2.0 * R * 2 * f * d),
+        "requant_hidden": ("hbm", R * f * 4 + R * f * q8),
+        "mmq_down": ("tensor", 2.0 * R * d * f),
+        "combine_topk": ("hbm", R * d * 4 + T * d * 4 + T * K * 8),
+    }
+    total_bytes = (T * d * 4 + 2 * R * d * q8 + 2 * R * f * 4 + 2 * R * f * q8 + 2 * R * d * 4
+                   + T * d * 4 + 6 * R * 4 + 3 * n_active * rec_bytes)
+    ops = 2.0 * R * 3 * f * d
+    return stages, total_bytes, ops
+
+
+# -------------------------------------------------------------- GPU arm --
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import quantized_routed_expert_q8_gb300 as m
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = mw.CONFIGS[args.config]
+    wl = mw.make_workload(cfg)
+    T, K, E, d, f = cfg.T, cfg.K, cfg.E, cfg.d, cfg.f
+    R = T * K
+    arena = torch.from_numpy(wl.arena).to(dev)
+    x = torch.from_numpy(wl.x).to(dev)
+    ids = torch.from_numpy(wl.ids).to(dev)
+    w = torch.from_numpy(wl.w).to(dev)
+    layer = m.MoeLayer(cfg.wtype, E, d, f, K, T, arena, wl.rec_bytes, wl.arena_stride, dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    stage_names = ["slot_map", "quantize_scatter", "group_gather", "mmq_gateup",
+                   "requant_hidden", "mmq_down", "combine_topk"]
+
+    def step(evs=None):
+        L = layer
+        calls = [
+            lambda: m.moe_build_slot_map(ids, E, L.offsets, L.slot, L.src, L.active, L.n_active,
+                                         L.ws),
+            lambda: m.moe_quantize_scatter_q8_1(x, L.slot, K, R, L.q, L.ds),
+            lambda: m.moe_group_gather_active(L.arena, L.rec_bytes, L.arena_stride, L.active,
+                                              L.n_active, E, L.group_buf, L.slot_stride),
+            lambda: m.moe_grouped_mmq_gateup(L.wtype, L.group_buf, L.slot_stride, L.active,
+                                             L.n_active, L.offsets, E, L.q, L.ds, R, d, f, L.h,
+                                             L.ws),
+            lambda: m.moe_requant_hidden_q8_1(L.h, R, f, L.hq, L.hds),
+            lambda: m.moe_grouped_mmq_down(L.wtype, L.group_buf, L.slot_stride, L.active,
+                                           L.n_active, L.offsets, E, L.hq, L.hds, R, d, f, L.y,
+                                           L.ws),
+            lambda: m.moe_combine_topk(L.y, R, L.slot, w, T, K, d, L.out),
+        ]
+        for i, c in enumerate(calls):
+            if evs is not None:
+                evs[i].record(stream)
+            c()
+        if evs is not None:
+            evs[len(calls)].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    assert m.moe_device_error(layer.ws) == 0
+    n_active = int(layer.n_active.item())
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = m.moe_launch_count()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        step(events[s])
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    launches = m.moe_launch_count() - launches0
+    clocks = sampler.stop() if sampler else None
+    stage_ms = np.array([[ev[i].elapsed_time(ev[i + 1]) for i in range(7)] for ev in events])
+    step_ms = stage_ms.sum(axis=1)
+    ms = float(step_ms.mean())
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API: pinned host inputs in, output out
+    hx = torch.from_numpy(wl.x).pin_memory()
+    hids = torch.from_numpy(wl.ids).pin_memory()
+    hw = torch.from_numpy(wl.w).pin_memory()
+    hout = torch.empty((T, d), dtype=torch.float32).pin_memory()
+    dx = torch.empty_like(x)
+    dids = torch.empty_like(ids)
+    dw = torch.empty_like(w)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dids.copy_(hids, non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        out = layer.forward(dx, dids, dw)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_ms = []
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms.append(a.elapsed_time(b))
+    e2e_ms = float(np.mean(e_ms))
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert m.moe_device_error(layer.ws) == 0
+
+    if rank != 0:
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+        return None
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    stages, total_bytes, ops = layer_accounting(cfg, n_active, wl.rec_bytes, R)
+    mean_stage = stage_ms.mean(axis=0)
+    phases = {n: round(float(v), 4) for n, v in zip(stage_names, mean_stage)}
+    dom = int(np.argmax(mean_stage))
+    dom_name = stage_names[dom]
+    bound, amount = stages[dom_name]
+    sec = mean_stage[dom] / 1e3
+    if bound == "hbm":
+        achieved, peak, unit = amount / sec / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = amount / sec / 1e12, tflops, "TFLOP/s"
+    t_roof = max(total_bytes / (hbm * 1e9), ops / (tflops * 1e12))
+    qs_sec = mean_stage[1] / 1e3
+    qs_gbs = stages["quantize_scatter"][1] / qs_sec / 1e9
+    value = world * T / (ms / 1e3)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8 x int8 block dots, fp32 scales and accumulation",
+        "data": "synthetic: seeded N(0,1) activations and router logits, N(0,0.02) weights "
+                "quantized to " + mw.WTYPE_NAMES[cfg.wtype],
+        "config": dict(cfg.describe(), l2="flushed between steps (512 MB write)",
+                       n_active_experts=n_active, mmq_path=mmq_path()),
+        "roofline": {"kernel": dom_name, "bound": bound, "achieved": round(achieved, 2),
+                     "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
+                     "traffic": None, "peak_source": f"{peak_src} ({'sustained' if bound == 'tensor' else 'copy'})"},
+        "layer_roofline": {"t_roofline_ms": round(t_roof * 1e3, 4),
+                           "frac": round(t_roof * 1e3 / ms, 4),
+                           "algorithmic_bytes": int(total_bytes), "ops": ops,
+                           "bound": "hbm" if total_bytes / hbm / 1e9 >= ops / tflops / 1e12 else "tensor"},
+        "quantize_scatter": {"GB/s": round(qs_gbs, 1), "frac_of_hbm": round(qs_gbs / hbm, 4),
+                             "bytes": int(stages["quantize_scatter"][1])},
+        "phases_ms": phases,
+        "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": int(wl.x.nbytes + wl.ids.nbytes + wl.w.nbytes),
+                "d2h_bytes_per_step": int(T * d * 4)},
+        "gpu_launches": int(launches),
+        "wall_s_timed": round(t_wall, 3),
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return line
+
+
+def mmq_path() -> str:
+    return "simt" if os.environ.get("MOE_MMQ_PATH") == "simt" else "default"
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def oracle_sample(wl, n_tokens: int, seed: int = 1):
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(wl.cfg.T, n_tokens, replace=False))
+    return wl.subset(toks)
+
+
+def time_oracle(wl, n_tokens):
+    import oracle
+    sub = oracle_sample(wl, n_tokens)
+    cfg = wl.cfg
+    t = time.perf_counter()
+    oracle.layer_forward(cfg.wtype, wl.arena, wl.rec_bytes, wl.arena_stride, sub.x, sub.ids, sub.w,
+                         cfg.E, cfg.d, cfg.f)
+    return time.perf_counter() - t
+
+
+def calibrate_tokens(wl, budget_s: float) -> int:
+    t4 = time_oracle(wl, 4)
+    n = int(4 * budget_s / max(t4, 1e-3))
+    return max(4, min(n, wl.cfg.T))
+
+
+def cpu_baseline(wl, budget_s: float = 15.0):
+    n = calibrate_tokens(wl, budget_s)
+    sec = time_oracle(wl, n)
+    return {"value": round(n / sec, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} seeded tokens of the {wl.cfg.T}-token workload with their routing "
+                      f"(all seven stages, single-threaded C, {sec:.1f} s)",
+            "host_cores": os.cpu_count()}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    cfg = mw.CONFIGS[args.config]
+    wl = mw.make_workload(cfg)
+    per_step = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    n = calibrate_tokens(wl, per_step)
+    for _ in range(args.warmup):
+        time_oracle(wl, n)
+    secs = [time_oracle(wl, n) for _ in range(args.steps)]
+    ms = 1e3 * float(np.mean(secs))
+    value = n / (ms / 1e3)
+    sample = (f"{n} seeded tokens of the {cfg.T}-token workload per step (all seven stages, "
+              f"single-threaded C oracle)")
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 x int8 block dots, fp32 scales and accumulation", "data": "synthetic",
+        "config": dict(cfg.describe(), sample_tokens=n), "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(mw.CONFIGS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        line = run_gpu(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,221 @@
+/*
+ * moe_q8.h -- C ABI of the GB300 quantized routed-expert MoE prefill library
+ * (libmoe_q8.so, CUDA kernels for sm_103a).
+ *
+ * One call per stage of a mixture-of-experts layer's prompt (prefill) step:
+ *   1. moe_build_slot_map         routing ids -> expert-sorted rows, slot/src maps
+ *   2. moe_quantize_scatter_q8_1  quantize each token once, write it to its K rows
+ *   3. moe_group_gather[_active]  copy up to 16 routed experts per launch
+ *   4. moe_grouped_mmq_gateup     int8 x quantized-weight block dots, SiLU(g)*u
+ *   5. moe_requant_hidden_q8_1    q8_1 re-quantization of the hidden rows
+ *   6. moe_grouped_mmq_down       down projection
+ *   7. moe_combine_topk           weighted sum of each token's K rows
+ *
+ * Sources (pull-request pages of the "Strata" engine):
+ *   [#1368] "prefill: quantize each token's MoE input once and scatter it to its
+ *           k rows (the same bytes)", intro and section "Identity".
+ *   [#439]  "prefill: a group's expert gathers in one launch (bit-identical, long
+ *           prompts +4%)", section "What".
+ *   [#372]  "Prompt path: an MMQ group's experts gathered in one launch, after one
+ *           wait, released by one event", "What changes".
+ *   [#1282] "prefill: STRATA_PREFILL_CPU_SHARE=auto hands a small chunk's
+ *           least-routed experts to the idle CPU pool", "What it does".
+ *
+ * Conventions shared by every call:
+ *   - Pointers are DEVICE pointers owned by the caller unless a parameter says
+ *     "host".  No call allocates, frees, synchronizes (except moe_device_error)
+ *     or keeps a pointer after it returns.  Every call is asynchronous on
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - Misuse that the host can see (null pointer with nonzero size, a width that
+ *     is not a multiple of 32, a misaligned buffer, too small a workspace, a
+ *     group larger than 16) returns an error status before anything is launched.
+ *   - A failed launch returns MOE_ERR_CUDA (the CUDA error is left for
+ *     cudaGetLastError to report as well).
+ *   - Data-dependent problems found on the device never trap: the kernels skip
+ *     the offending item, stay in bounds, and set a bit in the workspace's
+ *     error word, which moe_device_error reads back.
+ *   - Empty inputs (T = 0, R = 0, no active expert) are valid and do nothing
+ *     beyond writing the (empty) outputs' headers such as offsets.
+ *
+ * Formats:
+ *   q8_1 activations: 32-wide blocks.  d = amax/127 (fp32, IEEE division),
+ *     q = round-half-away-from-zero(x/d) (IEEE division) in int8, S = sum(q);
+ *     stored: q plane int8 [rows][width], ds plane [rows][width/32][2] of
+ *     binary16 bit patterns (d, s) with s = fp16(d * S).  An all-zero block is
+ *     q = 0, d = 0, s = 0.
+ *   Expert record (this library's layout): three matrices, gate [f x d], up
+ *     [f x d], down [d x f], each stored as: quant plane (rows x K, reduction
+ *     dimension innermost; Q8_0 int8; Q4_1 two 4-bit values per byte, byte j of
+ *     a block holding element 2j in the low nibble and 2j+1 in the high), then
+ *     the binary16 d plane [rows][K/32], then for Q4_1 the binary16 m plane
+ *     [rows][K/32].  Every plane starts on a 128-byte boundary.  Weight value
+ *     w = d*q (Q8_0) or d*q + m (Q4_1).
+ */
+#ifndef MOE_Q8_H
+#define MOE_Q8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1, /* null pointer, bad size or count */
+    MOE_ERR_ALIGNMENT = -2,   /* a buffer or stride is not aligned as required */
+    MOE_ERR_WORKSPACE = -3,   /* ws is null or smaller than moe_workspace_size */
+    MOE_ERR_UNSUPPORTED = -4, /* a size outside what the kernels support */
+    MOE_ERR_CUDA = -5,        /* a CUDA runtime or launch error */
+    MOE_ERR_DEVICE = -6       /* moe_device_error found a device-side error bit */
+} moe_status;
+
+typedef enum { MOE_W_Q8_0 = 0, MOE_W_Q4_1 = 1 } moe_wtype;
+
+/* Device error bits, set in the workspace error word. */
+#define MOE_DEV_ERR_BAD_EXPERT_ID 0x1u /* an id outside [0, E): its slot is -1 */
+#define MOE_DEV_ERR_BAD_ROWS 0x2u      /* offsets or slot beyond R: rows skipped */
+#define MOE_DEV_ERR_TIMEOUT 0x4u       /* a bounded wait inside a kernel gave up */
+
+/* Bytes of one expert record (gate, up, down) for the given weight type. */
+size_t moe_expert_record_bytes(int wtype, int d, int f);
+
+/* Byte offsets of the gate, up and down matrices inside a record. */
+void moe_expert_record_offsets(int wtype, int d, int f, size_t* gate, size_t* up, size_t* down);
+
+/* Workspace bytes the calls that take `ws` need for T tokens, top-K, E experts,
+   model width d and expert FFN width f.  The workspace must be 256-byte aligned
+   and is reused by every call; its first word is the device error word, which
+   must be zero before the first call (moe_workspace_init). */
+size_t moe_workspace_size(int T, int K, int E, int d, int f);
+
+/* Zero the workspace header (error word and counters), async on stream. */
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Stage 1 -- inverse routing map.  [#1368] intro: token t's k-th row is
+ * slot[t*K+k], the inverse of src (src[row] = token of that row).
+ *   ids      int32 [T*K], ids[t*K+k] = token t's k-th expert.
+ *   offsets  int32 [E+1] out: exclusive prefix sum of per-expert row counts;
+ *            expert e owns rows offsets[e] .. offsets[e+1]-1; offsets[E] = R.
+ *   slot     int32 [T*K] out: row of (t, k); within an expert rows follow
+ *            ascending t*K+k (a stable counting sort).  -1 for a dropped id.
+ *   src      int32 [T*K] out: src[row] = t for rows < R (entries >= R untouched).
+ *   active   int32 [E] out: experts with at least one row, ascending, then -1.
+ *   n_active int32 [1] out.
+ * Ids outside [0, E) are dropped and flag MOE_DEV_ERR_BAD_EXPERT_ID.
+ * Limits: 1 <= E <= 8192, T*K < 2^31.
+ */
+int moe_build_slot_map(const int32_t* ids, int T, int K, int E, int32_t* offsets, int32_t* slot,
+                       int32_t* src, int32_t* active, int32_t* n_active, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/*
+ * Stage 2 -- [#1368] intro: quantize each token's row of x once to q8_1 and
+ * write the blocks to all K of its rows slot[t*K+k] (the same bytes as the
+ * per-row gather quantizer).
+ *   x    float [T][d], 16-byte aligned.    slot int32 [T*K].
+ *   q    int8 [R][d] out, 8-byte aligned.  ds uint16 [R][d/32][2] out, 4-byte aligned.
+ * Rows with slot outside [0, R) are skipped.  d % 32 == 0.
+ */
+int moe_quantize_scatter_q8_1(const float* x, int T, int d, int K, const int32_t* slot, int R,
+                              int8_t* q, uint16_t* ds, void* stream);
+
+/*
+ * Stage 2, gather form -- the per-row quantizer the scatter replaces
+ * ([#1368] intro, mmq::quantize(x, src, ...)): row r quantizes token src[r].
+ * Same layouts and alignment as moe_quantize_scatter_q8_1; src values outside
+ * [0, T) leave the row unwritten.
+ */
+int moe_quantize_gather_q8_1(const float* x, int T, int d, const int32_t* src, int R, int8_t* q,
+                             uint16_t* ds, void* stream);
+
+/*
+ * Stage 3 -- [#439] "What" / [#372] "What changes": one launch copies up to 16
+ * experts' records into the group buffer, blockIdx.y = expert; expert j of the
+ * call lands in slot first_slot + j.  The same bytes as one copy per expert.
+ *   arena        device: expert e's record at arena + e*arena_stride.
+ *   expert_ids   HOST int32 [n], 1 <= n <= 16, first_slot + n <= 16.
+ *   group_buf    device: slot s at group_buf + s*slot_stride.
+ * 16-byte vector copies when arena, group_buf, rec_bytes and both strides are
+ * 16-byte aligned; otherwise a byte copy with the same result.  Source and
+ * destination must not overlap.
+ */
+int moe_group_gather(const uint8_t* arena, size_t rec_bytes, size_t arena_stride,
+                     const int32_t* expert_ids, int n, int first_slot, uint8_t* group_buf,
+                     size_t slot_stride, void* stream);
+
+/*
+ * Stage 3 for a whole layer without a host round trip: the groups of 16 active
+ * experts (ascending id, as listed by moe_build_slot_map) gathered back to
+ * back; the expert at active position p lands at group_base + p*slot_stride.
+ * One launch covers every group (blockIdx.y = expert within its group,
+ * blockIdx.z = group).  active and n_active are device pointers; max_active
+ * bounds n_active (normally E).
+ */
+int moe_group_gather_active(const uint8_t* arena, size_t rec_bytes, size_t arena_stride,
+                            const int32_t* active, const int32_t* n_active, int max_active,
+                            uint8_t* group_base, size_t slot_stride, void* stream);
+
+/*
+ * Stage 4 -- grouped quantized matmul, gate and up, then h = SiLU(g) * u.
+ * For the expert at active position p (record at group_base + p*slot_stride,
+ * expert id e = active[p]) and each of its rows r in [offsets[e], offsets[e+1]):
+ *   g[r,j] = sum over blocks b ascending of  dWg[j,b]*dx[r,b]*I_b (+ mWg[j,b]*sx[r,b]
+ *            for Q4_1), accumulated in fp32, I_b the exact integer block dot;
+ *   u likewise with W_up;  h[r,j] = (g / (1 + exp(-g))) * u.
+ *   q int8 [R][d], ds uint16 [R][d/32][2] (stage 2 output); h float [R][f] out.
+ * group_base and slot_stride must be 128-byte aligned, d % 32 == 0, f % 32 == 0.
+ * Rows past R are skipped (MOE_DEV_ERR_BAD_ROWS).
+ */
+int moe_grouped_mmq_gateup(int wtype, const uint8_t* group_base, size_t slot_stride,
+                           const int32_t* active, const int32_t* n_active, const int32_t* offsets,
+                           int E, const int8_t* q, const uint16_t* ds, int R, int d, int f,
+                           float* h, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Stage 5 -- the down-projection q8_1 quantization of the hidden rows ([#1368]
+ * intro calls it unchanged): hq int8 [R][f], hds uint16 [R][f/32][2] from
+ * h float [R][f].  Same quantizer as stage 2 with the identity row map.
+ */
+int moe_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
+                            void* stream);
+
+/*
+ * Stage 6 -- grouped quantized matmul, down projection: y[r,i] = sum over
+ * blocks b of dWd[i,b]*dh[r,b]*I_b (+ mWd[i,b]*sh[r,b] for Q4_1), fp32.
+ *   hq, hds from stage 5; y float [R][d] out.  Alignment as stage 4.
+ */
+int moe_grouped_mmq_down(int wtype, const uint8_t* group_base, size_t slot_stride,
+                         const int32_t* active, const int32_t* n_active, const int32_t* offsets,
+                         int E, const int8_t* hq, const uint16_t* hds, int R, int d, int f,
+                         float* y, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Stage 7 -- [#1282] "What it does": the combine weights each of a token's
+ * rows by its top-k weight:  out[t,i] = sum over k ascending of
+ * w[t*K+k] * y[slot[t*K+k], i], accumulated as acc = fma(w, y, acc) from 0.
+ * Rows with slot outside [0, R) add nothing.
+ *   y float [R][d], 16-byte aligned;  w float [T*K];  out float [T][d] out,
+ *   16-byte aligned.  d % 4 == 0.
+ */
+int moe_combine_topk(const float* y, int R, const int32_t* slot, const float* w, int T, int K,
+                     int d, float* out, void* stream);
+
+/* Synchronize `stream`, read the workspace error word into *bits (host) and
+   clear it.  Returns MOE_ERR_DEVICE if any bit was set, MOE_OK otherwise. */
+int moe_device_error(void* ws, uint32_t* bits, void* stream);
+
+/* Number of kernels the library has launched in this process (a diagnostic
+   counter for benchmarks; calls that return early launch nothing). */
+unsigned long long moe_launch_count(void);
+
+/* Human-readable text of a moe_status value. */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_Q8_H */

@@ -1,0 +1,265 @@
+"""GB300 quantized routed-expert (q8_1 MMQ) MoE prefill layer.
+
+A thin ctypes binding over ``libmoe_q8.so`` (hand-written CUDA for sm_103a; C ABI
+in ``include/moe_q8.h``).  Every function has the name of the C entry point it
+calls and only marshals arguments: torch tensors in, device pointers and sizes
+out, the current CUDA stream unless one is given.  All arithmetic runs in the
+library's kernels; there is no CPU fallback -- importing this package on a
+machine without the built library raises.
+
+``MoeLayer`` owns the per-layer device buffers and runs the seven stages in
+order on one stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe_q8.so")
+
+MOE_W_Q8_0 = 0
+MOE_W_Q4_1 = 1
+QK = 32
+
+DEV_ERR_BAD_EXPERT_ID = 0x1
+DEV_ERR_BAD_ROWS = 0x2
+DEV_ERR_TIMEOUT = 0x4
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_Z = ctypes.c_size_t
+_SIGNATURES = {
+    "moe_expert_record_bytes": (_Z, [_I, _I, _I]),
+    "moe_expert_record_offsets": (None, [_I, _I, _I, _P, _P, _P]),
+    "moe_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "moe_workspace_init": (_I, [_P, _Z, _P]),
+    "moe_build_slot_map": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_quantize_scatter_q8_1": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "moe_quantize_gather_q8_1": (_I, [_P, _I, _I, _P, _I, _P, _P, _P]),
+    "moe_group_gather": (_I, [_P, _Z, _Z, _P, _I, _I, _P, _Z, _P]),
+    "moe_group_gather_active": (_I, [_P, _Z, _Z, _P, _P, _I, _P, _Z, _P]),
+    "moe_grouped_mmq_gateup": (_I, [_I, _P, _Z, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_requant_hidden_q8_1": (_I, [_P, _I, _I, _P, _P, _P]),
+    "moe_grouped_mmq_down": (_I, [_I, _P, _Z, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_combine_topk": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
+    "moe_launch_count": (ctypes.c_ulonglong, []),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+}
+EXPORTED = tuple(_SIGNATURES)
+
+
+class MoeError(RuntimeError):
+    pass
+
+
+def lib():
+    """Load libmoe_q8.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        msg = lib().moe_status_string(rc).decode()
+        raise MoeError(f"{name} failed: {msg} ({rc})")
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors passed to libmoe_q8 must live on the GPU")
+
+
+# --- sizes ------------------------------------------------------------------
+
+def moe_expert_record_bytes(wtype: int, d: int, f: int) -> int:
+    return int(lib().moe_expert_record_bytes(wtype, d, f))
+
+
+def moe_expert_record_offsets(wtype: int, d: int, f: int):
+    g, u, dn = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    lib().moe_expert_record_offsets(wtype, d, f, ctypes.byref(g), ctypes.byref(u), ctypes.byref(dn))
+    return g.value, u.value, dn.value
+
+
+def moe_workspace_size(T: int, K: int, E: int, d: int, f: int) -> int:
+    return int(lib().moe_workspace_size(T, K, E, d, f))
+
+
+def moe_workspace_init(ws: torch.Tensor, stream=None):
+    _check(lib().moe_workspace_init(_p(ws), ws.numel() * ws.element_size(), _s(stream)),
+           "moe_workspace_init")
+
+
+# --- the seven stages ---------------------------------------------------------
+
+def moe_build_slot_map(ids, E, offsets, slot, src, active, n_active, ws, stream=None):
+    _dev(ids, offsets, slot, src, active, n_active, ws)
+    T, K = ids.shape
+    _check(lib().moe_build_slot_map(_p(ids), T, K, E, _p(offsets), _p(slot), _p(src), _p(active),
+                                    _p(n_active), _p(ws), ws.numel() * ws.element_size(), _s(stream)),
+           "moe_build_slot_map")
+
+
+def moe_quantize_scatter_q8_1(x, slot, K, R, q, ds, stream=None):
+    _dev(x, slot, q, ds)
+    T, d = x.shape
+    _check(lib().moe_quantize_scatter_q8_1(_p(x), T, d, K, _p(slot), R, _p(q), _p(ds), _s(stream)),
+           "moe_quantize_scatter_q8_1")
+
+
+def moe_quantize_gather_q8_1(x, src, R, q, ds, stream=None):
+    _dev(x, src, q, ds)
+    T, d = x.shape
+    _check(lib().moe_quantize_gather_q8_1(_p(x), T, d, _p(src), R, _p(q), _p(ds), _s(stream)),
+           "moe_quantize_gather_q8_1")
+
+
+def moe_group_gather(arena, rec_bytes, arena_stride, expert_ids, first_slot, group_buf,
+                     slot_stride, stream=None):
+    """expert_ids: host sequence of up to 16 ints (kernel parameters)."""
+    _dev(arena, group_buf)
+    ids = (ctypes.c_int32 * len(expert_ids))(*[int(e) for e in expert_ids])
+    _check(lib().moe_group_gather(_p(arena), rec_bytes, arena_stride, ctypes.cast(ids, _P),
+                                  len(expert_ids), first_slot, _p(group_buf), slot_stride,
+                                  _s(stream)), "moe_group_gather")
+
+
+def moe_group_gather_active(arena, rec_bytes, arena_stride, active, n_active, max_active,
+                            group_base, slot_stride, stream=None):
+    _dev(arena, active, n_active, group_base)
+    _check(lib().moe_group_gather_active(_p(arena), rec_bytes, arena_stride, _p(active),
+                                         _p(n_active), max_active, _p(group_base), slot_stride,
+                                         _s(stream)), "moe_group_gather_active")
+
+
+def moe_grouped_mmq_gateup(wtype, group_base, slot_stride, active, n_active, offsets, E, q, ds, R,
+                           d, f, h, ws, stream=None):
+    _dev(group_base, active, n_active, offsets, q, ds, h, ws)
+    _check(lib().moe_grouped_mmq_gateup(wtype, _p(group_base), slot_stride, _p(active), _p(n_active),
+                                        _p(offsets), E, _p(q), _p(ds), R, d, f, _p(h), _p(ws),
+                                        ws.numel() * ws.element_size(), _s(stream)),
+           "moe_grouped_mmq_gateup")
+
+
+def moe_requant_hidden_q8_1(h, R, f, hq, hds, stream=None):
+    _dev(h, hq, hds)
+    _check(lib().moe_requant_hidden_q8_1(_p(h), R, f, _p(hq), _p(hds), _s(stream)),
+           "moe_requant_hidden_q8_1")
+
+
+def moe_grouped_mmq_down(wtype, group_base, slot_stride, active, n_active, offsets, E, hq, hds, R,
+                         d, f, y, ws, stream=None):
+    _dev(group_base, active, n_active, offsets, hq, hds, y, ws)
+    _check(lib().moe_grouped_mmq_down(wtype, _p(group_base), slot_stride, _p(active), _p(n_active),
+                                      _p(offsets), E, _p(hq), _p(hds), R, d, f, _p(y), _p(ws),
+                                      ws.numel() * ws.element_size(), _s(stream)),
+           "moe_grouped_mmq_down")
+
+
+def moe_combine_topk(y, R, slot, w, T, K, d, out, stream=None):
+    _dev(y, slot, w, out)
+    _check(lib().moe_combine_topk(_p(y), R, _p(slot), _p(w), T, K, d, _p(out), _s(stream)),
+           "moe_combine_topk")
+
+
+def moe_device_error(ws, stream=None) -> int:
+    """Synchronize the stream and return (and clear) the workspace error bits."""
+    bits = ctypes.c_uint32(0)
+    rc = lib().moe_device_error(_p(ws), ctypes.byref(bits), _s(stream))
+    if rc not in (0, -6):
+        _check(rc, "moe_device_error")
+    return int(bits.value)
+
+
+def moe_launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().moe_launch_count())
+
+
+# --- one layer -------------------------------------------------------------------
+
+class MoeLayer:
+    """Device buffers of one MoE layer for up to ``T_max`` tokens, and the seven
+    calls in order.  ``arena`` holds the E expert records (uint8, on the GPU,
+    record e at e*arena_stride); it stays resident and is not copied per call
+    except by the group gather stage."""
+
+    def __init__(self, wtype, E, d, f, K, T_max, arena, rec_bytes, arena_stride, device=None):
+        device = device or arena.device
+        self.wtype, self.E, self.d, self.f, self.K, self.T_max = wtype, E, d, f, K, T_max
+        self.arena, self.rec_bytes, self.arena_stride = arena, rec_bytes, arena_stride
+        self.slot_stride = (rec_bytes + 255) // 256 * 256
+        R = T_max * K
+        i32 = dict(dtype=torch.int32, device=device)
+        self.offsets = torch.zeros(E + 1, **i32)
+        self.slot = torch.zeros(max(R, 1), **i32)
+        self.src = torch.zeros(max(R, 1), **i32)
+        self.active = torch.zeros(E, **i32)
+        self.n_active = torch.zeros(1, **i32)
+        self.q = torch.zeros((max(R, 1), d), dtype=torch.int8, device=device)
+        self.ds = torch.zeros((max(R, 1), d // QK, 2), dtype=torch.int16, device=device)
+        self.group_buf = torch.zeros(E * self.slot_stride, dtype=torch.uint8, device=device)
+        self.h = torch.zeros((max(R, 1), f), dtype=torch.float32, device=device)
+        self.hq = torch.zeros((max(R, 1), f), dtype=torch.int8, device=device)
+        self.hds = torch.zeros((max(R, 1), f // QK, 2), dtype=torch.int16, device=device)
+        self.y = torch.zeros((max(R, 1), d), dtype=torch.float32, device=device)
+        self.out = torch.zeros((max(T_max, 1), d), dtype=torch.float32, device=device)
+        ws_bytes = moe_workspace_size(T_max, K, E, d, f)
+        self.ws = torch.zeros((ws_bytes + 255) // 256 * 256, dtype=torch.uint8, device=device)
+        moe_workspace_init(self.ws)
+
+    def forward(self, x, ids, w, stream=None):
+        """x f32 [T, d], ids int32 [T, K], w f32 [T, K] on the GPU -> out [T, d]
+        (a view of the layer's output buffer)."""
+        T = x.shape[0]
+        assert T <= self.T_max and ids.shape == (T, self.K) and w.shape == (T, self.K)
+        K, E, d, f = self.K, self.E, self.d, self.f
+        R = T * K
+        moe_build_slot_map(ids, E, self.offsets, self.slot, self.src, self.active, self.n_active,
+                           self.ws, stream)
+        moe_quantize_scatter_q8_1(x, self.slot, K, R, self.q, self.ds, stream)
+        moe_group_gather_active(self.arena, self.rec_bytes, self.arena_stride, self.active,
+                                self.n_active, E, self.group_buf, self.slot_stride, stream)
+        moe_grouped_mmq_gateup(self.wtype, self.group_buf, self.slot_stride, self.active,
+                               self.n_active, self.offsets, E, self.q, self.ds, R, d, f, self.h,
+                               self.ws, stream)
+        moe_requant_hidden_q8_1(self.h, R, f, self.hq, self.hds, stream)
+        moe_grouped_mmq_down(self.wtype, self.group_buf, self.slot_stride, self.active,
+                             self.n_active, self.offsets, E, self.hq, self.hds, R, d, f, self.y,
+                             self.ws, stream)
+        moe_combine_topk(self.y, R, self.slot, w, T, K, d, self.out, stream)
+        return self.out[:T]

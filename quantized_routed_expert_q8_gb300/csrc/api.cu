@@ -1,0 +1,231 @@
+// C ABI of the library (declared in include/moe_q8.h): argument checks on the
+// host, then the stage launches.  Nothing here allocates or synchronizes
+// except moe_device_error.
+#include <cstdlib>
+#include <cstring>
+
+#include "common.cuh"
+#include "mmq.cuh"
+
+namespace moe {
+int launch_build_slot_map(const int32_t*, int, int, int, int32_t*, int32_t*, int32_t*, int32_t*,
+                          int32_t*, uint8_t*, cudaStream_t);
+int launch_quantize_scatter(const float*, int, int, int, const int32_t*, int, int8_t*, uint16_t*,
+                            cudaStream_t);
+int launch_quantize_gather(const float*, int, int, const int32_t*, int, int8_t*, uint16_t*,
+                           cudaStream_t);
+int launch_requant_hidden(const float*, int, int, int8_t*, uint16_t*, cudaStream_t);
+int launch_group_gather(const uint8_t*, size_t, size_t, const int32_t*, int, int, uint8_t*, size_t,
+                        cudaStream_t);
+int launch_group_gather_active(const uint8_t*, size_t, size_t, const int32_t*, const int32_t*, int,
+                               uint8_t*, size_t, cudaStream_t);
+int launch_combine_topk(const float*, int, const int32_t*, const float*, int, int, int, float*,
+                        cudaStream_t);
+int launch_mmq_simt(int, bool, const uint8_t*, size_t, const int32_t*, const int32_t*,
+                    const int32_t*, int, const int8_t*, const uint16_t*, int, int, int, float*,
+                    uint8_t*, const WsLayout&, cudaStream_t);
+int launch_mmq_tc(int, bool, const uint8_t*, size_t, const int32_t*, const int32_t*,
+                  const int32_t*, int, const int8_t*, const uint16_t*, int, int, int, float*,
+                  uint8_t*, const WsLayout&, cudaStream_t);
+bool mmq_tc_supported(int wtype, bool gateup, int d, int f);
+}  // namespace moe
+
+#include <atomic>
+
+namespace moe {
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool al(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+inline bool wtype_ok(int w) { return w == MOE_W_Q8_0 || w == MOE_W_Q4_1; }
+
+// MOE_MMQ_PATH=simt forces the CUDA-core MMQ (cross-check of the tensor-core path)
+inline bool force_simt() {
+    const char* v = std::getenv("MOE_MMQ_PATH");
+    return v && std::strcmp(v, "simt") == 0;
+}
+
+// recover the (T, K) the workspace was sized for is not possible; the MMQ and
+// slot-map calls size it from their own arguments
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (!ws) return MOE_ERR_WORKSPACE;
+    if (!al(ws, 256)) return MOE_ERR_ALIGNMENT;
+    if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+int mmq_common(int wtype, bool gateup, const uint8_t* group_base, size_t slot_stride,
+               const int32_t* active, const int32_t* n_active, const int32_t* offsets, int E,
+               const int8_t* xq, const uint16_t* xds, int R, int d, int f, float* out, void* ws,
+               size_t ws_bytes, void* stream) {
+    if (!wtype_ok(wtype) || R < 0 || d <= 0 || f <= 0 || E <= 0 || E > MAX_E)
+        return MOE_ERR_INVALID_ARG;
+    if (d % QK || f % QK) return MOE_ERR_INVALID_ARG;
+    if (!active || !n_active || !offsets) return MOE_ERR_INVALID_ARG;
+    if (R > 0 && (!group_base || !xq || !xds || !out)) return MOE_ERR_INVALID_ARG;
+    if (!al(group_base, 128) || slot_stride % 128) return MOE_ERR_ALIGNMENT;
+    if (!al(xq, 16) || !al(xds, 4) || !al(out, 16)) return MOE_ERR_ALIGNMENT;
+    // the tile list needs R/16 + E entries: size it as if T*K = R
+    WsLayout W = ws_layout(R, 1, E, d, f);
+    int rc = check_ws(ws, ws_bytes, W.total);
+    if (rc) return rc;
+    if (R == 0) return MOE_OK;
+    uint8_t* w8 = (uint8_t*)ws;
+    if (!force_simt() && mmq_tc_supported(wtype, gateup, d, f))
+        return launch_mmq_tc(wtype, gateup, group_base, slot_stride, active, n_active, offsets, E,
+                             xq, xds, R, d, f, out, w8, W, S(stream));
+    return launch_mmq_simt(wtype, gateup, group_base, slot_stride, active, n_active, offsets, E, xq,
+                           xds, R, d, f, out, w8, W, S(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_expert_record_bytes(int wtype, int d, int f) {
+    if (!wtype_ok(wtype) || d <= 0 || f <= 0 || d % QK || f % QK) return 0;
+    return rec_layout(wtype, d, f).bytes;
+}
+
+void moe_expert_record_offsets(int wtype, int d, int f, size_t* gate, size_t* up, size_t* down) {
+    RecLayout R = rec_layout(wtype, d, f);
+    if (gate) *gate = R.gate;
+    if (up) *up = R.up;
+    if (down) *down = R.down;
+}
+
+size_t moe_workspace_size(int T, int K, int E, int d, int f) {
+    if (T < 0 || K < 0 || E <= 0) return 0;
+    WsLayout a = ws_layout(T, K, E, d, f);
+    return a.total;
+}
+
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws || ws_bytes < 256) return MOE_ERR_WORKSPACE;
+    if (!al(ws, 256)) return MOE_ERR_ALIGNMENT;
+    return cudaMemsetAsync(ws, 0, 256, S(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_build_slot_map(const int32_t* ids, int T, int K, int E, int32_t* offsets, int32_t* slot,
+                       int32_t* src, int32_t* active, int32_t* n_active, void* ws,
+                       size_t ws_bytes, void* stream) {
+    if (T < 0 || K < 0 || E <= 0 || E > MAX_E) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * K >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    if (!offsets || !active || !n_active) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * K > 0 && (!ids || !slot || !src)) return MOE_ERR_INVALID_ARG;
+    int rc = check_ws(ws, ws_bytes, ws_layout(T, K, E, 0, 0).total);
+    if (rc) return rc;
+    return launch_build_slot_map(ids, T, K, E, offsets, slot, src, active, n_active, (uint8_t*)ws,
+                                 S(stream));
+}
+
+int moe_quantize_scatter_q8_1(const float* x, int T, int d, int K, const int32_t* slot, int R,
+                              int8_t* q, uint16_t* ds, void* stream) {
+    if (T < 0 || K < 0 || R < 0 || d <= 0 || d % QK) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * K > 0 && (!x || !slot)) return MOE_ERR_INVALID_ARG;
+    if (R > 0 && (!q || !ds)) return MOE_ERR_INVALID_ARG;
+    if (!al(x, 16) || !al(q, 8) || !al(ds, 4)) return MOE_ERR_ALIGNMENT;
+    if (T == 0 || K == 0 || R == 0) return MOE_OK;
+    return launch_quantize_scatter(x, T, d, K, slot, R, q, ds, S(stream));
+}
+
+int moe_quantize_gather_q8_1(const float* x, int T, int d, const int32_t* src, int R, int8_t* q,
+                             uint16_t* ds, void* stream) {
+    if (T < 0 || R < 0 || d <= 0 || d % QK) return MOE_ERR_INVALID_ARG;
+    if (R > 0 && (!x || !src || !q || !ds)) return MOE_ERR_INVALID_ARG;
+    if (!al(x, 16) || !al(q, 8) || !al(ds, 4)) return MOE_ERR_ALIGNMENT;
+    if (R == 0) return MOE_OK;
+    return launch_quantize_gather(x, T, d, src, R, q, ds, S(stream));
+}
+
+int moe_group_gather(const uint8_t* arena, size_t rec_bytes, size_t arena_stride,
+                     const int32_t* expert_ids, int n, int first_slot, uint8_t* group_buf,
+                     size_t slot_stride, void* stream) {
+    if (n < 1 || n > 16 || first_slot < 0 || first_slot + n > 16) return MOE_ERR_INVALID_ARG;
+    if (!arena || !expert_ids || !group_buf) return MOE_ERR_INVALID_ARG;
+    if (rec_bytes > arena_stride || rec_bytes > slot_stride) return MOE_ERR_INVALID_ARG;
+    for (int j = 0; j < n; ++j)
+        if (expert_ids[j] < 0) return MOE_ERR_INVALID_ARG;
+    return launch_group_gather(arena, rec_bytes, arena_stride, expert_ids, n, first_slot, group_buf,
+                               slot_stride, S(stream));
+}
+
+int moe_group_gather_active(const uint8_t* arena, size_t rec_bytes, size_t arena_stride,
+                            const int32_t* active, const int32_t* n_active, int max_active,
+                            uint8_t* group_base, size_t slot_stride, void* stream) {
+    if (max_active < 0 || max_active > MAX_E) return MOE_ERR_INVALID_ARG;
+    if (!arena || !active || !n_active || !group_base) return MOE_ERR_INVALID_ARG;
+    if (rec_bytes > arena_stride || rec_bytes > slot_stride) return MOE_ERR_INVALID_ARG;
+    return launch_group_gather_active(arena, rec_bytes, arena_stride, active, n_active, max_active,
+                                      group_base, slot_stride, S(stream));
+}
+
+int moe_grouped_mmq_gateup(int wtype, const uint8_t* group_base, size_t slot_stride,
+                           const int32_t* active, const int32_t* n_active, const int32_t* offsets,
+                           int E, const int8_t* q, const uint16_t* ds, int R, int d, int f,
+                           float* h, void* ws, size_t ws_bytes, void* stream) {
+    return mmq_common(wtype, true, group_base, slot_stride, active, n_active, offsets, E, q, ds, R,
+                      d, f, h, ws, ws_bytes, stream);
+}
+
+int moe_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
+                            void* stream) {
+    if (R < 0 || f <= 0 || f % QK) return MOE_ERR_INVALID_ARG;
+    if (R > 0 && (!h || !hq || !hds)) return MOE_ERR_INVALID_ARG;
+    if (!al(h, 16) || !al(hq, 8) || !al(hds, 4)) return MOE_ERR_ALIGNMENT;
+    if (R == 0) return MOE_OK;
+    return launch_requant_hidden(h, R, f, hq, hds, S(stream));
+}
+
+int moe_grouped_mmq_down(int wtype, const uint8_t* group_base, size_t slot_stride,
+                         const int32_t* active, const int32_t* n_active, const int32_t* offsets,
+                         int E, const int8_t* hq, const uint16_t* hds, int R, int d, int f,
+                         float* y, void* ws, size_t ws_bytes, void* stream) {
+    return mmq_common(wtype, false, group_base, slot_stride, active, n_active, offsets, E, hq, hds,
+                      R, d, f, y, ws, ws_bytes, stream);
+}
+
+int moe_combine_topk(const float* y, int R, const int32_t* slot, const float* w, int T, int K,
+                     int d, float* out, void* stream) {
+    if (T < 0 || K < 0 || R < 0 || d <= 0 || d % 4) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && !out) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * K > 0 && (!slot || !w)) return MOE_ERR_INVALID_ARG;
+    if (R > 0 && !y) return MOE_ERR_INVALID_ARG;
+    if (!al(y, 16) || !al(out, 16)) return MOE_ERR_ALIGNMENT;
+    if (T == 0) return MOE_OK;
+    return launch_combine_topk(y, R, slot, w, T, K, d, out, S(stream));
+}
+
+int moe_device_error(void* ws, uint32_t* bits, void* stream) {
+    if (!ws || !bits) return MOE_ERR_INVALID_ARG;
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, S(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    *bits = v;
+    if (v && cudaMemsetAsync(ws, 0, 4, S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+unsigned long long moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_ALIGNMENT: return "misaligned buffer or stride";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_UNSUPPORTED: return "unsupported size";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE: return "device-side error flag set";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

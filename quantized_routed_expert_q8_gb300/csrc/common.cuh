@@ -1,0 +1,91 @@
+// Shared definitions of the CUDA library: record layout, workspace layout,
+// device error word.  Used only by the library's own .cu files.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_q8.h"
+
+namespace moe {
+
+constexpr int QK = 32;  // block width of q8_1, Q8_0 and Q4_1
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// One weight matrix of an expert record: quant plane, fp16 d plane [rows][K/32],
+// fp16 m plane (Q4_1) -- each plane 128-byte aligned.
+struct MatLayout {
+    size_t q, d, m, bytes;
+};
+
+__host__ __device__ inline MatLayout mat_layout(int wtype, int rows, int k) {
+    MatLayout L;
+    size_t qb = (size_t)rows * (size_t)k / (wtype == MOE_W_Q4_1 ? 2 : 1);
+    size_t sb = (size_t)rows * (size_t)(k / QK) * 2;
+    L.q = 0;
+    L.d = align_up(qb, 128);
+    L.m = L.d + align_up(sb, 128);
+    L.bytes = L.m + (wtype == MOE_W_Q4_1 ? align_up(sb, 128) : 0);
+    return L;
+}
+
+// gate [f x d], up [f x d], down [d x f]
+struct RecLayout {
+    size_t gate, up, down, bytes;
+    MatLayout gu, dn;
+};
+
+__host__ __device__ inline RecLayout rec_layout(int wtype, int d, int f) {
+    RecLayout R;
+    R.gu = mat_layout(wtype, f, d);
+    R.dn = mat_layout(wtype, d, f);
+    R.gate = 0;
+    R.up = R.gu.bytes;
+    R.down = 2 * R.gu.bytes;
+    R.bytes = 2 * R.gu.bytes + R.dn.bytes;
+    return R;
+}
+
+// Workspace: [header 256 B: error word, counters][slot-map chunk counts]
+//            [tile list][spare]
+constexpr int SLOT_CHUNK = 1024;  // (t,k) entries per slot-map chunk
+constexpr int MAX_E = 8192;
+
+struct WsLayout {
+    size_t err;           // uint32 error word
+    size_t counters;      // uint32 counters[48]
+    size_t chunk_counts;  // int32 [n_chunks][E]
+    size_t tiles;         // int4 [max_tiles]
+    size_t total;
+    int n_chunks;
+    int max_tiles;
+};
+
+inline WsLayout ws_layout(int T, int K, int E, int d, int f) {
+    (void)d;
+    (void)f;
+    WsLayout W;
+    long long TK = (long long)T * K;
+    W.err = 0;
+    W.counters = 64;
+    W.chunk_counts = 256;
+    W.n_chunks = (int)((TK + SLOT_CHUNK - 1) / SLOT_CHUNK);
+    size_t cc = align_up((size_t)W.n_chunks * (size_t)E * 4, 256);
+    W.tiles = W.chunk_counts + cc;
+    // smallest row tile of any MMQ schedule is 16 rows; one partial tile per expert
+    W.max_tiles = (int)(TK / 16 + E + 16);
+    W.total = W.tiles + align_up((size_t)W.max_tiles * 16, 256) + 256;
+    return W;
+}
+
+// Number of kernels this library has launched (diagnostics for benchmarks).
+void count_launches(int n);
+
+__device__ inline void set_error(uint32_t* err, uint32_t bit) {
+    if (err) atomicOr(err, bit);
+}
+
+}  // namespace moe

@@ -1,0 +1,19 @@
+// Declarations shared by the grouped MMQ kernels and the C-ABI layer.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// indices into the workspace counter array (uint32 counters[48])
+enum { MMQ_COUNTER_NTILES = 0, MMQ_COUNTER_TICKET = 1 };
+
+int launch_mmq_tiles(const int32_t* active, const int32_t* n_active, const int32_t* offsets,
+                     int E, int R, int BM, uint8_t* ws, const WsLayout& W, cudaStream_t stream);
+
+// SiLU(g) * u in fp32 with SiLU(g) = g / (1 + exp(-g)), IEEE division.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+}  // namespace moe

@@ -1,0 +1,78 @@
+"""Host-side checks of the C ABI (no GPU needed): the built library loads and
+exports every function include/moe_q8.h declares, the binding covers them, and
+size queries agree with the record layout of the oracle and the generator."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_workloads as mw
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_q8.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_routed_expert_q8_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_covers_header():
+    import quantized_routed_expert_q8_gb300 as m
+    assert sorted(m.EXPORTED) == _declared()
+    for n in _declared():
+        assert callable(getattr(m, n, None)) or n == "moe_status_string", n
+
+
+@pytest.mark.parametrize("wtype", [0, 1])
+def test_record_bytes_agree(lib, wtype):
+    import quantized_routed_expert_q8_gb300 as m
+    for d, f in ((256, 128), (2048, 768), (96, 64)):
+        assert m.moe_expert_record_bytes(wtype, d, f) == oracle.expert_record_bytes(wtype, d, f)
+        assert m.moe_expert_record_bytes(wtype, d, f) == mw.record_bytes(wtype, d, f)
+        assert m.moe_expert_record_offsets(wtype, d, f) == oracle.record_offsets(wtype, d, f)
+    assert m.moe_expert_record_bytes(wtype, 100, 64) == 0  # d not a multiple of 32
+
+
+def test_status_strings(lib):
+    import quantized_routed_expert_q8_gb300 as m
+    L = m.lib()
+    for rc in range(0, -7, -1):
+        assert L.moe_status_string(rc)
+    assert m.moe_workspace_size(8192, 10, 512, 2048, 768) > 0
+
+
+def test_host_checks_reject_before_launch(lib):
+    """Host-visible misuse returns an error status without touching the GPU."""
+    import quantized_routed_expert_q8_gb300 as m
+    L = m.lib()
+    P = ctypes.c_void_p
+    # null stream is fine: nothing launches on these paths
+    assert L.moe_group_gather(P(16), 16, 16, P(16), 17, 0, P(16), 16, None) == -1
+    assert L.moe_group_gather(P(16), 16, 16, P(16), 2, 15, P(16), 16, None) == -1
+    assert L.moe_quantize_scatter_q8_1(P(16), 4, 100, 2, P(16), 8, P(16), P(16), None) == -1
+    assert L.moe_quantize_scatter_q8_1(P(17), 4, 64, 2, P(16), 8, P(16), P(16), None) == -2
+    assert L.moe_build_slot_map(P(16), 4, 2, 8, P(16), P(16), P(16), P(16), P(16), None, 0,
+                                None) == -3
+    assert L.moe_build_slot_map(P(16), 4, 2, 0, P(16), P(16), P(16), P(16), P(16), P(256), 1 << 20,
+                                None) == -1
+    assert L.moe_grouped_mmq_gateup(0, P(128), 100, P(16), P(16), P(16), 4, P(16), P(16), 8, 64,
+                                    64, P(16), P(256), 1 << 20, None) == -2
+    assert L.moe_combine_topk(P(16), 8, P(16), P(16), 2, 2, 6, P(16), None) == -1

@@ -1,0 +1,320 @@
+"""GPU parity: every stage of the CUDA library against the CPU oracle on the same
+seeded inputs, through the C ABI (the ctypes binding).
+
+Bars: bit-exact for the slot map, the q8_1 bytes, the gathered group buffers,
+the re-quantized hidden bytes and the combine (given identical inputs); the
+stage-level fp32 matmul outputs within 1e-5 relative L2 per row (they differ at
+most by the last bits of exp in SiLU); the layer output within 2e-3 relative L2
+per token, all-zero tokens exactly zero.  Full-size workloads are checked on
+sampled rows / tokens the oracle computes one by one (each token depends only on
+its own rows).
+"""
+import numpy as np
+import pytest
+
+import moe_workloads as mw
+import oracle
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import quantized_routed_expert_q8_gb300 as m  # noqa: E402
+
+ALL = [c.name for c in mw.CONFIG_LIST]
+SMALL = [mw.TINY.name, mw.T600.name]
+
+
+def _ws(T, K, E, d, f):
+    n = m.moe_workspace_size(T, K, E, d, f)
+    ws = torch.zeros((n + 255) // 256 * 256, dtype=torch.uint8, device="cuda")
+    m.moe_workspace_init(ws)
+    return ws
+
+
+def _slot_map_gpu(ids, E):
+    T, K = ids.shape
+    R = T * K
+    dev = dict(dtype=torch.int32, device="cuda")
+    off = torch.zeros(E + 1, **dev)
+    slot = torch.full((max(R, 1),), -7, **dev)
+    src = torch.full((max(R, 1),), -7, **dev)
+    act = torch.zeros(E, **dev)
+    na = torch.zeros(1, **dev)
+    ws = _ws(T, K, E, 64, 64)
+    m.moe_build_slot_map(H.to_dev(ids), E, off, slot, src, act, na, ws)
+    bits = m.moe_device_error(ws)
+    return dict(offsets=off.cpu().numpy(), slot=slot.cpu().numpy()[:R], src=src.cpu().numpy(),
+                active=act.cpu().numpy(), n_active=int(na.item()), bits=bits)
+
+
+# ----------------------------------------------------------------- stage 1 --
+
+@pytest.mark.parametrize("name", ALL)
+def test_slot_map(name):
+    wl = H.workload(name)
+    E = wl.cfg.E
+    g = _slot_map_gpu(wl.ids, E)
+    o = oracle.build_slot_map(wl.ids, E)
+    R = int(o["offsets"][E])
+    assert g["bits"] == 0
+    assert np.array_equal(g["offsets"], o["offsets"])
+    assert np.array_equal(g["slot"], o["slot"])
+    assert np.array_equal(g["src"][:R], o["src"])
+    assert g["n_active"] == o["n_active"]
+    assert np.array_equal(g["active"], o["active"])
+
+
+@pytest.mark.parametrize("T,K,E", [(1, 1, 1), (2, 10, 512), (1000, 3, 7), (3000, 8, 8192), (5, 4, 4)])
+def test_slot_map_shapes(T, K, E):
+    rng = np.random.default_rng(T + K + E)
+    ids = rng.integers(0, E, (T, K)).astype(np.int32)
+    g = _slot_map_gpu(ids, E)
+    o = oracle.build_slot_map(ids, E)
+    assert np.array_equal(g["offsets"], o["offsets"]) and np.array_equal(g["slot"], o["slot"])
+    assert np.array_equal(g["active"], o["active"]) and g["n_active"] == o["n_active"]
+
+
+def test_slot_map_bad_ids_flagged():
+    ids = np.array([[0, 3], [7, -1], [2, 3], [3, 100]], np.int32)
+    g = _slot_map_gpu(ids, 4)
+    o = oracle.build_slot_map(ids, 4)
+    assert g["bits"] & m.DEV_ERR_BAD_EXPERT_ID
+    assert np.array_equal(g["slot"], o["slot"]) and np.array_equal(g["offsets"], o["offsets"])
+
+
+def test_slot_map_empty():
+    g = _slot_map_gpu(np.zeros((0, 4), np.int32), 8)
+    assert g["n_active"] == 0 and not g["offsets"].any() and (g["active"] == -1).all()
+
+
+# ----------------------------------------------------------------- stage 2 --
+
+def _quant_gpu(x, slot, K, R):
+    T, d = x.shape
+    q = torch.full((max(R, 1), d), 0x55, dtype=torch.int8, device="cuda")
+    ds = torch.full((max(R, 1), d // 32, 2), 0x55, dtype=torch.int16, device="cuda")
+    m.moe_quantize_scatter_q8_1(H.to_dev(x), H.to_dev(slot), K, R, q, ds)
+    return q.cpu().numpy()[:R], H.u16(ds)[:R]
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_quantize_scatter(name):
+    wl = H.workload(name)
+    cfg = wl.cfg
+    o = oracle.build_slot_map(wl.ids, cfg.E)
+    R = int(o["offsets"][cfg.E])
+    q, ds = _quant_gpu(wl.x, o["slot"], cfg.K, R)
+    qo, dso = oracle.quantize_scatter_q8_1(wl.x, o["slot"], cfg.K, R)
+    assert np.array_equal(q, qo)
+    assert np.array_equal(ds, dso)
+    for t in cfg.zero_list():
+        rows = o["slot"][t * cfg.K:(t + 1) * cfg.K]
+        assert not q[rows].any() and not ds[rows].any()
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 600, 2099])
+def test_scatter_equals_gather_on_gpu(T):
+    """Identity of the scatter and the per-row gather quantizer, both on the GPU
+    (10 of 512 experts, one all-zero token), and against the oracle."""
+    d, K, E = 2048, 10, 512
+    x = mw.normal_f32(0x77 + T, 1, T * d).reshape(T, d)
+    x[T // 3] = 0.0
+    ids, _ = mw.topk_softmax(mw.normal_f32(0x77 + T, 2, T * E).reshape(T, E), K)
+    o = oracle.build_slot_map(ids, E)
+    R = T * K
+    qs, dss = _quant_gpu(x, o["slot"], K, R)
+    q = torch.zeros((R, d), dtype=torch.int8, device="cuda")
+    ds = torch.zeros((R, d // 32, 2), dtype=torch.int16, device="cuda")
+    m.moe_quantize_gather_q8_1(H.to_dev(x), H.to_dev(o["src"]), R, q, ds)
+    assert np.array_equal(qs, q.cpu().numpy()) and np.array_equal(dss, H.u16(ds))
+    qo, dso = oracle.quantize_gather_q8_1(x, o["src"])
+    assert np.array_equal(qs, qo) and np.array_equal(dss, dso)
+
+
+def test_quantizer_golden_blocks_on_gpu():
+    from tests.test_oracle_pins import _golden_blocks
+    cases = _golden_blocks()
+    x = np.stack([c["x"] for c in cases]).reshape(len(cases), 32)
+    x = np.concatenate([x, np.zeros((len(cases), 32), np.float32)], 1)  # width 64
+    R = len(cases)
+    slot = np.arange(R, dtype=np.int32)
+    q, ds = _quant_gpu(x, slot, 1, R)
+    for i, c in enumerate(cases):
+        assert np.array_equal(q[i, :32], c["q"]), c["name"]
+        assert ds[i, 0, 0] == c["d"] and ds[i, 0, 1] == c["s"], c["name"]
+
+
+def test_quantize_skips_rows_out_of_range():
+    x = mw.normal_f32(5, 1, 4 * 64).reshape(4, 64)
+    slot = np.array([0, 5, 2, -1, 3, 99, 1, 4], np.int32)
+    q, ds = _quant_gpu(x, slot, 2, 6)
+    qo, dso = oracle.quantize_scatter_q8_1(x, np.where((slot >= 0) & (slot < 6), slot, -1), 2, 6,
+                                           fill=0x55)
+    assert np.array_equal(q, qo) and np.array_equal(ds, dso)
+
+
+# ----------------------------------------------------------------- stage 3 --
+
+@pytest.mark.parametrize("rec,off", [(16 * 1000, 0), (16 * 1000 + 7, 0), (1, 0), (4096, 3)])
+def test_group_gather_batches(rec, off):
+    """#439: the batch equals one copy per expert for 1-16 experts, mid-group
+    starts, odd sizes and unaligned addresses."""
+    rng = np.random.default_rng(rec + off)
+    E, stride = 40, rec + (16 if off == 0 and rec % 16 == 0 else 5)
+    raw = rng.integers(0, 256, off + E * stride, dtype=np.uint8)
+    arena_h = raw[off:]
+    arena_d_raw = H.to_dev(raw)
+    arena_d = arena_d_raw[off:]
+    slot_stride = rec + (48 if rec % 16 == 0 else 9)
+    for n in (1, 2, 7, 15, 16):
+        for first in sorted({0, 1, 16 - n}):
+            if first + n > 16:
+                continue
+            ids = rng.choice(E, n, replace=False).astype(np.int32)
+            init = rng.integers(0, 256, 16 * slot_stride, dtype=np.uint8)
+            buf = H.to_dev(init)
+            m.moe_group_gather(arena_d, rec, stride, list(ids), first, buf, slot_stride)
+            ref = init.copy()
+            oracle.group_gather(arena_h, rec, stride, ids, first, ref, slot_stride)
+            assert np.array_equal(buf.cpu().numpy(), ref), (n, first)
+
+
+def test_group_gather_rejects_bad_groups():
+    a = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    b = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(m.MoeError):
+        m.moe_group_gather(a, 16, 16, list(range(17)), 0, b, 16)
+    with pytest.raises(m.MoeError):
+        m.moe_group_gather(a, 16, 16, [0, 1], 15, b, 16)
+
+
+@pytest.mark.parametrize("name", SMALL + [mw.T8192.name])
+def test_group_gather_active(name):
+    wl = H.workload(name)
+    cfg = wl.cfg
+    o = oracle.build_slot_map(wl.ids, cfg.E)
+    ss = (wl.rec_bytes + 255) // 256 * 256
+    gb = torch.zeros(cfg.E * ss, dtype=torch.uint8, device="cuda")
+    m.moe_group_gather_active(H.to_dev(wl.arena), wl.rec_bytes, wl.arena_stride,
+                              H.to_dev(o["active"]), H.to_dev(np.array([o["n_active"]], np.int32)),
+                              cfg.E, gb, ss)
+    ref = oracle.gather_groups(wl.arena, wl.rec_bytes, wl.arena_stride, o["active"], o["n_active"], ss)
+    n = o["n_active"] * ss
+    assert np.array_equal(gb.cpu().numpy()[:n], ref[:n])
+
+
+# --------------------------------------------------------------- stages 4-6 --
+
+def _mmq_gpu(stage, wl, o, xq, xds):
+    cfg = wl.cfg
+    E, d, f = cfg.E, cfg.d, cfg.f
+    R = int(o["offsets"][E])
+    ss = (wl.rec_bytes + 255) // 256 * 256
+    gb = torch.zeros(max(o["n_active"], 1) * ss, dtype=torch.uint8, device="cuda")
+    act = H.to_dev(o["active"])
+    na = H.to_dev(np.array([o["n_active"]], np.int32))
+    m.moe_group_gather_active(H.to_dev(wl.arena), wl.rec_bytes, wl.arena_stride, act, na, E, gb, ss)
+    ws = _ws(R, 1, E, d, f)
+    n = f if stage == "gateup" else d
+    out = torch.full((max(R, 1), n), float("nan"), dtype=torch.float32, device="cuda")
+    fn = m.moe_grouped_mmq_gateup if stage == "gateup" else m.moe_grouped_mmq_down
+    fn(cfg.wtype, gb, ss, act, na, H.to_dev(o["offsets"]), E, H.to_dev(xq),
+       H.to_dev(xds.view(np.int16)), R, d, f, out, ws)
+    assert m.moe_device_error(ws) == 0
+    return out.cpu().numpy()[:R]
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_mmq_gateup(name):
+    wl = H.workload(name)
+    cfg = wl.cfg
+    o = oracle.build_slot_map(wl.ids, cfg.E)
+    R = int(o["offsets"][cfg.E])
+    q, ds = oracle.quantize_scatter_q8_1(wl.x, o["slot"], cfg.K, R)
+    h = _mmq_gpu("gateup", wl, o, q, ds)
+    assert np.isfinite(h).all()
+    rows = np.arange(R) if R <= 64 else H.sample_rows(o["offsets"], o["active"], o["n_active"], 96, 1)
+    ref = H.oracle_rows("gateup", wl, o["offsets"], q, ds, rows)
+    err = H.rel_l2_rows(h[rows], ref)
+    assert err.max() <= 1e-5, err.max()
+    for t in cfg.zero_list():
+        assert not h[o["slot"][t * cfg.K:(t + 1) * cfg.K]].any()
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_mmq_down(name):
+    wl = H.workload(name)
+    cfg = wl.cfg
+    o = oracle.build_slot_map(wl.ids, cfg.E)
+    R = int(o["offsets"][cfg.E])
+    # hidden rows from the generator (scaled like SiLU(g)*u), quantized by the oracle
+    hid = mw.normal_f32(cfg.seed, 9, R * cfg.f, scale=0.05).reshape(R, cfg.f)
+    hid[::53] = 0.0
+    hq, hds = oracle.requant_hidden_q8_1(hid)
+    y = _mmq_gpu("down", wl, o, hq, hds)
+    rows = np.arange(R) if R <= 64 else H.sample_rows(o["offsets"], o["active"], o["n_active"], 96, 2)
+    ref = H.oracle_rows("down", wl, o["offsets"], hq, hds, rows)
+    err = H.rel_l2_rows(y[rows], ref)
+    assert err.max() <= 1e-5, err.max()
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_requant_hidden(name):
+    cfg = mw.CONFIGS[name]
+    R = min(cfg.T * cfg.K, 200000)
+    hid = mw.normal_f32(cfg.seed, 10, R * cfg.f, scale=0.05).reshape(R, cfg.f)
+    hid[::31] = 0.0
+    hid[5, :32] = np.float32(2.0 ** -130)
+    hq = torch.zeros((R, cfg.f), dtype=torch.int8, device="cuda")
+    hds = torch.zeros((R, cfg.f // 32, 2), dtype=torch.int16, device="cuda")
+    m.moe_requant_hidden_q8_1(H.to_dev(hid), R, cfg.f, hq, hds)
+    ro, rdo = oracle.requant_hidden_q8_1(hid)
+    assert np.array_equal(hq.cpu().numpy(), ro) and np.array_equal(H.u16(hds), rdo)
+
+
+# ----------------------------------------------------------------- stage 7 --
+
+@pytest.mark.parametrize("name", ALL)
+def test_combine(name):
+    wl = H.workload(name)
+    cfg = wl.cfg
+    o = oracle.build_slot_map(wl.ids, cfg.E)
+    R = int(o["offsets"][cfg.E])
+    y = mw.normal_f32(cfg.seed, 11, R * cfg.d).reshape(R, cfg.d)
+    out = torch.zeros((cfg.T, cfg.d), dtype=torch.float32, device="cuda")
+    m.moe_combine_topk(H.to_dev(y), R, H.to_dev(o["slot"]), H.to_dev(wl.w), cfg.T, cfg.K, cfg.d, out)
+    ref = oracle.combine_topk(y, o["slot"], wl.w, cfg.T, cfg.K, cfg.d)
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+# -------------------------------------------------------------- end to end --
+
+@pytest.mark.parametrize("name", ALL)
+def test_layer_end_to_end(name):
+    """The seven calls in order (MoeLayer) against the oracle on every token of
+    the small workloads and on sampled tokens (all-zero ones included) of the
+    large ones: <= 2e-3 relative L2 per token, zero tokens exactly zero."""
+    wl = H.workload(name)
+    cfg = wl.cfg
+    layer = m.MoeLayer(cfg.wtype, cfg.E, cfg.d, cfg.f, cfg.K, cfg.T, H.to_dev(wl.arena),
+                       wl.rec_bytes, wl.arena_stride)
+    out = layer.forward(H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w)).cpu().numpy()
+    assert m.moe_device_error(layer.ws) == 0
+    assert np.isfinite(out).all()
+    if cfg.T <= 600:
+        toks = np.arange(cfg.T)
+    else:
+        rng = np.random.default_rng(cfg.seed)
+        toks = np.unique(np.concatenate([rng.integers(0, cfg.T, 40), cfg.zero_list()[:4],
+                                         [0, cfg.T - 1]])).astype(np.int64)
+    sub = wl.subset(toks)
+    ref = oracle.layer_forward(cfg.wtype, wl.arena, wl.rec_bytes, wl.arena_stride, sub.x, sub.ids,
+                               sub.w, cfg.E, cfg.d, cfg.f)["out"]
+    err = H.rel_l2_rows(out[toks], ref)
+    assert err.max() <= 2e-3, (err.max(), toks[np.argmax(err)])
+    for t in cfg.zero_list():
+        assert not out[t].any()
