@@ -47,9 +47,10 @@
  *     [f x d], down [d x f], each stored as: quant plane (rows x K, reduction
  *     dimension innermost; Q8_0 int8; Q4_1 two 4-bit values per byte, byte j of
  *     a block holding element 2j in the low nibble and 2j+1 in the high), then
- *     the binary16 d plane [rows][K/32], then for Q4_1 the binary16 m plane
- *     [rows][K/32].  Every plane starts on a 128-byte boundary.  Weight value
- *     w = d*q (Q8_0) or d*q + m (Q4_1).
+ *     the binary16 d plane [K/32][rows] (block-major: the scale of row j, block
+ *     b is entry b*rows + j), then for Q4_1 the binary16 m plane [K/32][rows].
+ *     Every plane starts on a 128-byte boundary.  Weight value w = d*q (Q8_0)
+ *     or d*q + m (Q4_1).
  */
 #ifndef MOE_Q8_H
 #define MOE_Q8_H

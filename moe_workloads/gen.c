@@ -110,7 +110,8 @@ void gen_normal_f32(uint64_t seed, uint64_t tensor_id, uint64_t start, size_t n,
 
 /* ---------------- expert records (the library's weight format) --------------- */
 /* gate [f x d], up [f x d], down [d x f]; per matrix: quant plane, fp16 d plane
-   [rows x K/32], Q4_1 also fp16 m plane; planes 128-byte aligned. */
+   [K/32][rows] (block-major), Q4_1 also fp16 m plane [K/32][rows]; planes
+   128-byte aligned. */
 static size_t a128(size_t x) { return (x + 127u) & ~(size_t)127u; }
 
 static size_t mat_bytes(int wtype, int rows, int k, size_t* qoff, size_t* doff, size_t* moff) {
@@ -155,7 +156,7 @@ static void pack_matrix(int wtype, const float* w, int rows, int k, uint8_t* dst
                     x = fminf(127.0f, fmaxf(-127.0f, x));
                     q[i] = (int8_t)x;
                 }
-                dp[(size_t)r * nb + b] = to_f16_bits(dd);
+                dp[(size_t)b * rows + r] = to_f16_bits(dd);
             } else { /* Q4_1: d = (max-min)/15, m = min, q = round((w-m)/d) in [0,15] */
                 float mn = v[0], mx = v[0];
                 for (int i = 1; i < 32; ++i) {
@@ -172,8 +173,8 @@ static void pack_matrix(int wtype, const float* w, int rows, int k, uint8_t* dst
                     }
                     q[j] = (uint8_t)(lo | (hi << 4));
                 }
-                dp[(size_t)r * nb + b] = to_f16_bits(dd);
-                mp[(size_t)r * nb + b] = to_f16_bits(mn);
+                dp[(size_t)b * rows + r] = to_f16_bits(dd);
+                mp[(size_t)b * rows + r] = to_f16_bits(mn);
             }
         }
     }

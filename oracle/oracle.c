@@ -28,6 +28,8 @@
  *   q8_1 activations: 32-wide blocks, d = amax/127 stored as fp16,
  *                     q = round-half-away-from-zero(x/d), s = d * sum(q) as fp16.
  *   Q8_0 weights:     32-wide blocks, int8 q, fp16 d, w = d*q.
+ *                     (scale planes are block-major: the d of row j, block b
+ *                     is entry b*rows + j)
  *   Q4_1 weights:     32-wide blocks, 4-bit unsigned q (two per byte: byte j holds
  *                     element 2j in its low nibble, 2j+1 in its high nibble),
  *                     fp16 d and fp16 m, w = d*q + m; the MMQ uses s for the m term.
@@ -114,8 +116,9 @@ void oracle_f16_to_f32_array(const uint16_t* in, size_t n, float* out) {
 /* Expert record layout (this library's own format; the pages do not define  */
 /* one).  A record holds three matrices in the order gate [f x d], up [f x d], */
 /* down [d x f]; each matrix is the plane of quants (row-major, reduction dim */
-/* innermost), then the fp16 d plane [rows x K/32], then for Q4_1 the fp16 m  */
-/* plane; every plane starts on a 128-byte boundary.                          */
+/* innermost), then the fp16 d plane [K/32][rows] (block-major), then for     */
+/* Q4_1 the fp16 m plane [K/32][rows]; every plane starts on a 128-byte       */
+/* boundary.                                                                  */
 /* ------------------------------------------------------------------------- */
 static size_t align128(size_t x) { return (x + 127u) & ~(size_t)127u; }
 
@@ -288,8 +291,9 @@ void oracle_group_gather(const uint8_t* arena, size_t rec_bytes, size_t arena_st
 /*         and, for Q4_1, then fmaf(fp32(mW[b]), fp32(sX[b]), acc),            */
 /*   with I_b the exact integer sum over the block of qW * qX.                 */
 /* ------------------------------------------------------------------------- */
-static float mmq_dot(int wtype, const uint8_t* wq_row, const uint16_t* wd_row,
-                     const uint16_t* wm_row, const int8_t* xq_row, const uint16_t* xds_row, int k) {
+static float mmq_dot(int wtype, const uint8_t* wq_row, const uint16_t* wd, const uint16_t* wm,
+                     size_t sstride, const int8_t* xq_row, const uint16_t* xds_row, int k) {
+    /* wd / wm point at block 0 of this row; block b is sstride entries further */
     float acc = 0.0f;
     for (int b = 0; b < k / QK; ++b) {
         int32_t I = 0;
@@ -304,10 +308,11 @@ static float mmq_dot(int wtype, const uint8_t* wq_row, const uint16_t* wd_row,
                 I += lo * (int32_t)xb[2 * j] + hi * (int32_t)xb[2 * j + 1];
             }
         }
-        float scale = oracle_f16_to_f32(wd_row[b]) * oracle_f16_to_f32(xds_row[2 * b]);
+        float scale = oracle_f16_to_f32(wd[(size_t)b * sstride]) * oracle_f16_to_f32(xds_row[2 * b]);
         acc = fmaf(scale, (float)I, acc);
         if (wtype == ORACLE_W_Q4_1)
-            acc = fmaf(oracle_f16_to_f32(wm_row[b]), oracle_f16_to_f32(xds_row[2 * b + 1]), acc);
+            acc = fmaf(oracle_f16_to_f32(wm[(size_t)b * sstride]), oracle_f16_to_f32(xds_row[2 * b + 1]),
+                       acc);
     }
     return acc;
 }
@@ -317,7 +322,7 @@ typedef struct {
     const uint16_t* d;
     const uint16_t* m;
     size_t q_row; /* bytes per row of the quant plane */
-    int nb;       /* blocks per row */
+    int rows;     /* rows of the matrix = stride between blocks of a scale plane */
 } wmat;
 
 static wmat weight_matrix(int wtype, const uint8_t* base, int rows, int k) {
@@ -327,13 +332,12 @@ static wmat weight_matrix(int wtype, const uint8_t* base, int rows, int k) {
     W.d = (const uint16_t*)(base + L.d);
     W.m = (const uint16_t*)(base + L.m);
     W.q_row = (size_t)k / (wtype == ORACLE_W_Q4_1 ? 2u : 1u);
-    W.nb = k / QK;
+    W.rows = rows;
     return W;
 }
 
 static float wdot(int wtype, wmat W, int j, const int8_t* xq, const uint16_t* xds, int k) {
-    return mmq_dot(wtype, W.q + (size_t)j * W.q_row, W.d + (size_t)j * W.nb,
-                   W.m + (size_t)j * W.nb, xq, xds, k);
+    return mmq_dot(wtype, W.q + (size_t)j * W.q_row, W.d + j, W.m + j, (size_t)W.rows, xq, xds, k);
 }
 
 /* SiLU(g) * u in fp32, SiLU(g) = g / (1 + exp(-g)). */

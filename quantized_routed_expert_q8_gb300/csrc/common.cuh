@@ -15,8 +15,10 @@ constexpr int QK = 32;  // block width of q8_1, Q8_0 and Q4_1
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// One weight matrix of an expert record: quant plane, fp16 d plane [rows][K/32],
-// fp16 m plane (Q4_1) -- each plane 128-byte aligned.
+// One weight matrix of an expert record: quant plane [rows][K] (Q4_1: two
+// values per byte), fp16 d plane [K/32][rows] (block-major, so one block's
+// scales for consecutive rows are contiguous), fp16 m plane [K/32][rows] for
+// Q4_1 -- each plane 128-byte aligned.
 struct MatLayout {
     size_t q, d, m, bytes;
 };

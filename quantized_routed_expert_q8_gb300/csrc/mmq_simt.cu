@@ -50,8 +50,8 @@ __device__ __forceinline__ void load_w_tile(const uint8_t* __restrict__ qplane,
                     ws[tid][2 * h + 1] = (int)w1;
                 }
             }
-            dw[tid] = __half2float(dplane[(size_t)j * (k / QK) + b]);
-            mw[tid] = WT == MOE_W_Q4_1 ? __half2float(mplane[(size_t)j * (k / QK) + b]) : 0.0f;
+            dw[tid] = __half2float(dplane[(size_t)b * nrows + j]);  // block-major scales
+            mw[tid] = WT == MOE_W_Q4_1 ? __half2float(mplane[(size_t)b * nrows + j]) : 0.0f;
         } else {
 #pragma unroll
             for (int w = 0; w < 8; ++w) ws[tid][w] = 0;

@@ -264,11 +264,12 @@ def _planes(wtype, rec, off, rows, k):
         q = np.empty((rows, k), np.int64)
         q[:, 0::2] = p & 0x0F
         q[:, 1::2] = p >> 4
-    dpl = base[a128(qb):a128(qb) + sb].view(np.float16).reshape(rows, k // 32).astype(np.float64)
+    # scale planes are block-major [k/32][rows]
+    dpl = base[a128(qb):a128(qb) + sb].view(np.float16).reshape(k // 32, rows).T.astype(np.float64)
     mpl = None
     if wtype == mw.Q4_1:
         o = a128(qb) + a128(sb)
-        mpl = base[o:o + sb].view(np.float16).reshape(rows, k // 32).astype(np.float64)
+        mpl = base[o:o + sb].view(np.float16).reshape(k // 32, rows).T.astype(np.float64)
     return q, dpl, mpl
 
 
