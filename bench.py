@@ -50,54 +50,120 @@ def load_peaks():
 # ------------------------------------------------------------------ clocks --
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled every 5 ms through NVML (the
+    driver's libnvidia-ml, via ctypes) while the timed region runs; falls back
+    to nvidia-smi (200 ms) when NVML cannot be loaded."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, pci_bus_id: str | None = None):
         self.index = index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+        self.pci = pci_bus_id
+        self.samples = []
+        self.max_mhz = 0.0
+        self.reasons = set()
+        self._stop = None
+        self._thread = None
+        self._smi = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        rc = 1
+        if self.pci:  # the device this process uses, whatever CUDA_VISIBLE_DEVICES says
+            rc = lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci.encode(), ctypes.byref(h))
+        if rc != 0 and lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return lib, h, fn
 
     def start(self):
+        import ctypes
+        import threading
+        try:
+            lib, h, reasons_fn = self._nvml()
+        except (OSError, AttributeError):
+            self._start_smi()
+            return
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self._stop = threading.Event()
+
+        def loop():
+            clk = ctypes.c_uint()
+            rs = ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                    self.samples.append(float(clk.value))
+                if reasons_fn(h, ctypes.byref(rs)) == 0:
+                    for bit, name in self.REASONS.items():
+                        if rs.value & bit:
+                            self.reasons.add(name)
+                self._stop.wait(0.005)
+
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
+
+    def _start_smi(self):
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+        fields = ("index,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+            self._smi = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={fields}",
                  "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+        except OSError:
+            self._smi = None
 
     def stop(self):
-        if self.proc is None:
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=2)
+            src = "nvml"
+        elif self._smi is not None:
+            self._smi.terminate()
+            try:
+                self._smi.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._smi.kill()
+            self.fh.close()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            with open(self.path) as fh:
+                for line in fh:
+                    parts = [p.strip() for p in line.split(",")]
+                    try:
+                        self.samples.append(float(parts[1]))
+                        self.max_mhz = max(self.max_mhz, float(parts[2]))
+                    except (ValueError, IndexError):
+                        continue
+                    for n, v in zip(names, parts[3:7]):
+                        if v.lower() == "active":
+                            self.reasons.add(n)
+            os.unlink(self.path)
+            src = "nvidia-smi"
+        else:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.fh.close()
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as fh:
-            for line in fh:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx = max(mx, float(parts[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
+        if not self.samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples), "source": src}
+
+
+def pci_bus_id(dev):
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    try:
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except AttributeError:
+        return None
 
 
 # ------------------------------------------------------------ bytes / ops --
@@ -181,7 +247,7 @@ def run_gpu(args, rank, world, local_rank):
     n_active = int(layer.n_active.item())
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
-    sampler = ClockSampler(local_rank) if rank == 0 else None
+    sampler = ClockSampler(local_rank, pci_bus_id(dev)) if rank == 0 else None
     if sampler:
         sampler.start()
     if dist:
@@ -310,6 +376,63 @@ def mmq_path() -> str:
     return "simt" if os.environ.get("MOE_MMQ_PATH") == "simt" else "default"
 
 
+def run_stage(args):
+    """One stage of the layer, timed alone on its own inputs (a full layer is run
+    once first to produce them).  Used for profiler captures of one kernel."""
+    import torch
+
+    import quantized_routed_expert_q8_gb300 as m
+
+    cfg = mw.CONFIGS[args.config]
+    wl = mw.make_workload(cfg)
+    T, K, E, d, f = cfg.T, cfg.K, cfg.E, cfg.d, cfg.f
+    R = T * K
+    dev = torch.device("cuda", 0)
+    arena = torch.from_numpy(wl.arena).to(dev)
+    x = torch.from_numpy(wl.x).to(dev)
+    ids = torch.from_numpy(wl.ids).to(dev)
+    w = torch.from_numpy(wl.w).to(dev)
+    L = m.MoeLayer(cfg.wtype, E, d, f, K, T, arena, wl.rec_bytes, wl.arena_stride, dev)
+    L.forward(x, ids, w)
+    calls = {
+        "quantize_scatter": lambda: m.moe_quantize_scatter_q8_1(x, L.slot, K, R, L.q, L.ds),
+        "group_gather": lambda: m.moe_group_gather_active(L.arena, L.rec_bytes, L.arena_stride,
+                                                          L.active, L.n_active, E, L.group_buf,
+                                                          L.slot_stride),
+        "mmq_gateup": lambda: m.moe_grouped_mmq_gateup(L.wtype, L.group_buf, L.slot_stride,
+                                                       L.active, L.n_active, L.offsets, E, L.q,
+                                                       L.ds, R, d, f, L.h, L.ws),
+        "requant_hidden": lambda: m.moe_requant_hidden_q8_1(L.h, R, f, L.hq, L.hds),
+        "mmq_down": lambda: m.moe_grouped_mmq_down(L.wtype, L.group_buf, L.slot_stride, L.active,
+                                                   L.n_active, L.offsets, E, L.hq, L.hds, R, d, f,
+                                                   L.y, L.ws),
+        "combine_topk": lambda: m.moe_combine_topk(L.y, R, L.slot, w, T, K, d, L.out),
+    }
+    fn = calls[args.stage]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        fn()
+    ms = []
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert m.moe_device_error(L.ws) == 0
+    n_active = int(L.n_active.item())
+    stages, _, _ = layer_accounting(cfg, n_active, wl.rec_bytes, R)
+    bound, amount = stages[args.stage]
+    t = float(np.mean(ms)) / 1e3
+    rate = amount / t / (1e9 if bound == "hbm" else 1e12)
+    return {"stage": args.stage, "config": cfg.describe(), "ms": round(t * 1e3, 4),
+            "bound": bound, "achieved": round(rate, 2),
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "n_active_experts": n_active}
+
+
 # ------------------------------------------------------------- CPU oracle --
 
 def oracle_sample(wl, n_tokens: int, seed: int = 1):
@@ -379,12 +502,17 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage", default=None,
+                    help="time one stage alone (for profiler captures): quantize_scatter, "
+                         "mmq_gateup, mmq_down, requant_hidden, combine_topk, group_gather")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
+    if args.stage:
+        line = run_stage(args)
+    elif args.impl == "reference":
         line = run_reference(args, rank)
     else:
         line = run_gpu(args, rank, world, local_rank)
