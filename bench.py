@@ -384,10 +384,25 @@ def run_stage(args):
     import quantized_routed_expert_q8_gb300 as m
 
     cfg = mw.CONFIGS[args.config]
-    wl = mw.make_workload(cfg)
     T, K, E, d, f = cfg.T, cfg.K, cfg.E, cfg.d, cfg.f
     R = T * K
     dev = torch.device("cuda", 0)
+    if args.stage == "quantize_scatter":
+        # only the quantizer's own buffers: x, slot, q, ds (keeps profiler captures small)
+        x = torch.from_numpy(mw.activations(cfg)).to(dev)
+        ids_h, _ = mw.topk_softmax(mw.routing_logits(cfg), K)
+        ids = torch.from_numpy(ids_h).to(dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        off, slot, src = torch.zeros(E + 1, **i32), torch.zeros(R, **i32), torch.zeros(R, **i32)
+        act, na = torch.zeros(E, **i32), torch.zeros(1, **i32)
+        ws = torch.zeros(m.moe_workspace_size(T, K, E, d, f), dtype=torch.uint8, device=dev)
+        m.moe_workspace_init(ws)
+        m.moe_build_slot_map(ids, E, off, slot, src, act, na, ws)
+        q = torch.empty((R, d), dtype=torch.int8, device=dev)
+        ds = torch.empty((R, d // 32, 2), dtype=torch.int16, device=dev)
+        return _time_stage(args, cfg, lambda: m.moe_quantize_scatter_q8_1(x, slot, K, R, q, ds),
+                           ws, int(na.item()), 0)
+    wl = mw.make_workload(cfg)
     arena = torch.from_numpy(wl.arena).to(dev)
     x = torch.from_numpy(wl.x).to(dev)
     ids = torch.from_numpy(wl.ids).to(dev)
@@ -408,8 +423,15 @@ def run_stage(args):
                                                    L.y, L.ws),
         "combine_topk": lambda: m.moe_combine_topk(L.y, R, L.slot, w, T, K, d, L.out),
     }
-    fn = calls[args.stage]
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    return _time_stage(args, cfg, calls[args.stage], L.ws, int(L.n_active.item()), wl.rec_bytes)
+
+
+def _time_stage(args, cfg, fn, ws, n_active, rec_bytes):
+    import torch
+
+    import quantized_routed_expert_q8_gb300 as m
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     for _ in range(args.warmup):
         fn()
     ms = []
@@ -422,9 +444,8 @@ def run_stage(args):
         b.record()
         torch.cuda.synchronize()
         ms.append(a.elapsed_time(b))
-    assert m.moe_device_error(L.ws) == 0
-    n_active = int(L.n_active.item())
-    stages, _, _ = layer_accounting(cfg, n_active, wl.rec_bytes, R)
+    assert m.moe_device_error(ws) == 0
+    stages, _, _ = layer_accounting(cfg, n_active, rec_bytes, cfg.T * cfg.K)
     bound, amount = stages[args.stage]
     t = float(np.mean(ms)) / 1e3
     rate = amount / t / (1e9 if bound == "hbm" else 1e12)
