@@ -167,7 +167,9 @@ int moe_group_gather_active(const uint8_t* arena, size_t rec_bytes, size_t arena
  *            for Q4_1), accumulated in fp32, I_b the exact integer block dot;
  *   u likewise with W_up;  h[r,j] = (g / (1 + exp(-g))) * u.
  *   q int8 [R][d], ds uint16 [R][d/32][2] (stage 2 output); h float [R][f] out.
- * group_base and slot_stride must be 128-byte aligned, d % 32 == 0, f % 32 == 0.
+ * group_base and slot_stride must be 128-byte aligned, q, ds and h 16-byte
+ * aligned, d % 32 == 0, f % 32 == 0.  Shapes with d % 256 == 0 and f % 128 == 0
+ * run on the tensor cores; others on a CUDA-core kernel with the same result.
  * Rows past R are skipped (MOE_DEV_ERR_BAD_ROWS).
  */
 int moe_grouped_mmq_gateup(int wtype, const uint8_t* group_base, size_t slot_stride,

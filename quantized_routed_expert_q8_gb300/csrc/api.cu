@@ -70,7 +70,7 @@ int mmq_common(int wtype, bool gateup, const uint8_t* group_base, size_t slot_st
     if (!active || !n_active || !offsets) return MOE_ERR_INVALID_ARG;
     if (R > 0 && (!group_base || !xq || !xds || !out)) return MOE_ERR_INVALID_ARG;
     if (!al(group_base, 128) || slot_stride % 128) return MOE_ERR_ALIGNMENT;
-    if (!al(xq, 16) || !al(xds, 4) || !al(out, 16)) return MOE_ERR_ALIGNMENT;
+    if (!al(xq, 16) || !al(xds, 16) || !al(out, 16)) return MOE_ERR_ALIGNMENT;
     // the tile list needs R/16 + E entries: size it as if T*K = R
     WsLayout W = ws_layout(R, 1, E, d, f);
     int rc = check_ws(ws, ws_bytes, W.total);

@@ -1,14 +1,703 @@
-// Stages 4 and 6 on the tensor cores (tcgen05): not yet enabled.
+// Stages 4 and 6 on the fifth-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// The MMQ product of the pull-request pages ("#439 prefill: a group's expert
+// gathers in one launch", "What": the MMQ group's products run on the gathered
+// group buffers; "#1368 ...", intro: the q8_1 activations are expert-sorted
+// rows) is, for the expert at active position p and its rows r:
+//     acc[r, j] = sum over 32-blocks b of  dW[j,b] * dx[r,b] * I_b[r,j]
+//                 (+ mW[j,b] * sx[r,b] for Q4_1),    I_b = exact int dot of the block.
+// sm_103a has no integer tensor-core MMA, so each block's integer dot is formed
+// exactly by an fp16 MMA with fp32 accumulation: |q| <= 127 is exact in fp16,
+// each product is an integer below 2^14 and a block's sum stays below 2^24,
+// so every partial sum the tensor core forms is an exactly representable
+// integer.  The per-block fp32 scaling then runs on the CUDA cores in the same
+// order as the scalar definition: acc = fma(dW*dx, I_b, acc) (+ fma(mW, sx, acc)).
+//
+// One persistent CTA per SM (static round-robin over the device-built,
+// longest-first work list).  A work item is 128 tokens of one expert times two
+// 128-row weight blocks (gate and up rows j0..j0+127 for stage 4; down rows
+// i0..i0+255 for stage 6).  Warp roles:
+//   warp 0      TMA producer: raw int8 / 4-bit tiles and fp16 scales, 4 blocks a stage
+//   warp 1      MMA issuer: per 32-block, 2 x (M=128, N<=128, K=16) per matrix into
+//               one of two TMEM buffers, committed to an mbarrier
+//   warps 2-9   workers: for block b, read the partials out of TMEM, scale and
+//               accumulate in registers; then convert block b+2's raw tiles into
+//               the fp16 operand layout for the MMA.
+// Every wait is bounded: on timeout the kernel sets MOE_DEV_ERR_TIMEOUT, drains
+// what it started and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "mmq.cuh"
 
 namespace moe {
+namespace tc {
 
-bool mmq_tc_supported(int, bool, int, int) { return false; }
+constexpr int BN = 128;      // tokens per work item (TMEM columns per matrix)
+constexpr int BM = 128;      // weight rows per matrix (TMEM lanes)
+constexpr int KBS = 4;       // 32-blocks per raw stage
+constexpr int RS = 3;        // raw stages
+constexpr int NF = 2;        // fp16 operand slots = TMEM partial buffers
+constexpr int NSC = 4;       // scale ring slots
+constexpr int NWORK = 8;     // worker warps
+constexpr int THREADS = 32 * (2 + NWORK);
+constexpr int LOOKAHEAD = 2; // blocks converted ahead of the epilogue
+constexpr long long TIMEOUT_CYCLES = 1LL << 32;
 
-int launch_mmq_tc(int, bool, const uint8_t*, size_t, const int32_t*, const int32_t*, const int32_t*,
-                  int, const int8_t*, const uint16_t*, int, int, int, float*, uint8_t*,
-                  const WsLayout&, cudaStream_t) {
-    return MOE_ERR_UNSUPPORTED;
+constexpr int F16_A = 2 * BM * 64;  // two 128-row matrices x 32 fp16
+constexpr int F16_B = BN * 64;
+constexpr int F16_SLOT = F16_A + F16_B;
+constexpr int SC_SLOT = (2 * BM * 2 + BN * 2) * 4;  // dW, mW [256]; dX, sX [128] (fp32)
+
+__host__ __device__ constexpr int cround(int x, int a) { return (x + a - 1) / a * a; }
+
+template <int WT>
+struct Lay {
+    static constexpr int WROW = WT == MOE_W_Q8_0 ? 128 : 64;  // raw weight bytes per row per stage
+    static constexpr int W_RAW = 2 * BM * WROW;
+    static constexpr int X_RAW = BN * 128;
+    static constexpr int WS_RAW = 2 * KBS * BM * 2;
+    static constexpr int WM_RAW = WT == MOE_W_Q4_1 ? WS_RAW : 0;
+    static constexpr int XS_RAW = BN * KBS * 4;
+    static constexpr int O_W = 0;
+    static constexpr int O_X = W_RAW;
+    static constexpr int O_WS = O_X + X_RAW;
+    static constexpr int O_WM = O_WS + WS_RAW;
+    static constexpr int O_XS = O_WM + WM_RAW;
+    static constexpr int STAGE = cround(O_XS + XS_RAW, 1024);
+    static constexpr uint32_t TX = W_RAW + X_RAW + WS_RAW + WM_RAW + XS_RAW;
+    static constexpr int O_F16 = RS * STAGE;
+    static constexpr int O_SC = O_F16 + NF * F16_SLOT;
+    static constexpr int O_BAR = O_SC + NSC * SC_SLOT;
+    static constexpr int N_BARS = 2 * RS + 3 * NF;
+    static constexpr int SMEM = O_BAR + N_BARS * 8 + 16 + 1024;  // + alignment slack
+};
+
+// ------------------------------------------------------------------ PTX ----
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+            bar),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; false on abort or timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > TIMEOUT_CYCLES) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_2d(const CUtensorMap* m, uint32_t bar, uint32_t dst, int c0,
+                                       int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+        "%4}], [%2];" ::"r"(dst),
+        "l"(m), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_3d(const CUtensorMap* m, uint32_t bar, uint32_t dst, int c0,
+                                       int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+        "%4, %5}], [%2];" ::"r"(dst),
+        "l"(m), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_4d(const CUtensorMap* m, uint32_t bar, uint32_t dst, int c0,
+                                       int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+        "%4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(m), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: no swizzle, K-major core matrices of
+// 8 rows x 16 bytes; lbo = byte step between K-adjacent core matrices, sbo =
+// byte step between 8-row groups.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version of the tcgen05 family
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M x N.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// fp16 pair with bits 0x64XX holds 1024 + XX; subtract a constant pair
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
+    __half2 x = *reinterpret_cast<__half2*>(&a);
+    __half2 y = *reinterpret_cast<__half2*>(&b);
+    __half2 r = __hsub2(x, y);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+constexpr uint32_t MAGIC = 0x64646464u;    // 0x64 high bytes: fp16 1024 + low byte
+constexpr uint32_t H1152 = 0x64806480u;    // fp16 (1152, 1152)
+constexpr uint32_t H1024 = 0x64006400u;    // fp16 (1024, 1024)
+
+// 4 int8 (one word) -> fp16 pairs (q0,q1), (q2,q3), in element order
+__device__ __forceinline__ void cvt_i8x4(uint32_t w, uint32_t& h01, uint32_t& h23) {
+    uint32_t u = w ^ 0x80808080u;  // q + 128 as unsigned bytes
+    h01 = hsub2_bits(prmt(u, MAGIC, 0x4140u), H1152);
+    h23 = hsub2_bits(prmt(u, MAGIC, 0x4342u), H1152);
+}
+
+// 8 int8 in two words -> fp16 pairs in the order (x0,x4) (x1,x5) (x2,x6) (x3,x7),
+// the within-8 order the 4-bit weights unpack to
+__device__ __forceinline__ void cvt_i8x8_interleaved(uint32_t a, uint32_t b, uint32_t (&h)[4]) {
+    uint32_t ua = a ^ 0x80808080u, ub = b ^ 0x80808080u;
+    uint32_t t0 = prmt(ua, ub, 0x5140u), t1 = prmt(ua, ub, 0x7362u);
+    h[0] = hsub2_bits(prmt(t0, MAGIC, 0x4140u), H1152);
+    h[1] = hsub2_bits(prmt(t0, MAGIC, 0x4342u), H1152);
+    h[2] = hsub2_bits(prmt(t1, MAGIC, 0x4140u), H1152);
+    h[3] = hsub2_bits(prmt(t1, MAGIC, 0x4342u), H1152);
+}
+
+// 8 nibbles (byte j = element 2j low, 2j+1 high) -> (e0,e4) (e1,e5) (e2,e6) (e3,e7)
+__device__ __forceinline__ void cvt_u4x8(uint32_t w, uint32_t (&h)[4]) {
+    h[0] = hsub2_bits((w & 0x000F000Fu) | H1024, H1024);
+    h[1] = hsub2_bits(((w >> 4) & 0x000F000Fu) | H1024, H1024);
+    h[2] = hsub2_bits(((w >> 8) & 0x000F000Fu) | H1024, H1024);
+    h[3] = hsub2_bits(((w >> 12) & 0x000F000Fu) | H1024, H1024);
+}
+
+// byte offset of (row, 16-byte chunk c) in the fp16 K-major operand layout:
+// [row/8][chunk 0..3][row%8][16 B]  (lbo = 128, sbo = 512)
+__device__ __forceinline__ uint32_t f16_off(int row, int c) {
+    return (uint32_t)((row >> 3) * 512 + c * 128 + (row & 7) * 16);
+}
+
+struct Params {
+    const int4* tiles;
+    const int32_t* n_tiles;
+    int mt_count;  // weight-row tiles per token tile
+    int nb;        // 32-blocks of the reduction
+    int n_out;     // output row length (f for gate/up, d for down)
+    float* out;
+    uint32_t* err;
+};
+
+struct Item {
+    int p, r0, rows, ncols, w0;  // slot, first row, valid rows, MMA N, first weight row
+};
+
+template <bool GU>
+__device__ __forceinline__ Item load_item(const Params& P, int it) {
+    int tile = it / P.mt_count, mt = it - tile * P.mt_count;
+    int4 t = P.tiles[tile];
+    Item I;
+    I.p = t.x;
+    I.r0 = t.y;
+    I.rows = t.z;
+    I.ncols = (t.z + 15) & ~15;
+    I.w0 = GU ? mt * BM : mt * 2 * BM;
+    return I;
+}
+
+template <int WT, bool GU>
+__global__ void __maxnreg__(200)  // 320 threads x 200 registers fit one CTA per SM
+    mmq_tc_kernel(const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mWs,
+                  const __grid_constant__ CUtensorMap mWm, const __grid_constant__ CUtensorMap mX,
+                  const __grid_constant__ CUtensorMap mXs, const Params P) {
+    using L = Lay<WT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = (uint64_t*)(smem + L::O_BAR);
+    uint32_t* tmem_slot = (uint32_t*)(smem + L::O_BAR + L::N_BARS * 8);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    // barrier indices
+    const int B_RAW_FULL = 0, B_RAW_EMPTY = RS, B_F16_FULL = 2 * RS, B_TM_FULL = 2 * RS + NF,
+              B_TM_EMPTY = 2 * RS + 2 * NF;
+
+    const int n_items = *P.n_tiles * P.mt_count;
+    if ((int)blockIdx.x >= n_items) return;
+    const int my_items = (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+    const int nb = P.nb;
+    const int spi = nb / KBS;  // raw stages per item
+    const int total = my_items * nb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RS; ++i) {
+            mbar_init(bar(B_RAW_FULL + i), 1);
+            mbar_init(bar(B_RAW_EMPTY + i), NWORK * 32);
+        }
+        for (int i = 0; i < NF; ++i) {
+            mbar_init(bar(B_F16_FULL + i), NWORK * 32);
+            mbar_init(bar(B_TM_FULL + i), 1);
+            mbar_init(bar(B_TM_EMPTY + i), NWORK * 32);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_u32(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int gs = 0; gs < my_items * spi; ++gs) {
+                const int i = gs / spi, s = gs - i * spi;
+                const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
+                const int sl = gs % RS, u = gs / RS;
+                if (u > 0 && !mbar_wait(bar(B_RAW_EMPTY + sl), (u - 1) & 1, abort_flag)) break;
+                const uint32_t st = sbase + sl * L::STAGE;
+                const uint32_t fb = bar(B_RAW_FULL + sl);
+                mbar_expect_tx(fb, L::TX);
+                if (GU) {
+                    tma_4d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, 0, I.p);
+                    tma_4d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, 0, I.p);
+                    if (WT == MOE_W_Q4_1) tma_4d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, 0, I.p);
+                } else {
+                    tma_3d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, I.p);
+                    tma_3d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, I.p);
+                    if (WT == MOE_W_Q4_1) tma_3d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, I.p);
+                }
+                tma_2d(&mX, fb, st + L::O_X, s * 128, I.r0);
+                tma_2d(&mXs, fb, st + L::O_XS, s * KBS, I.r0);
+                issued = gs + 1;
+            }
+            // drain: every stage issued must have landed before the CTA may exit
+            for (int gs = (issued > RS ? issued - RS : 0); gs < issued; ++gs) {
+                long long t0 = clock64();
+                while (!mbar_try_wait(bar(B_RAW_FULL + gs % RS), (gs / RS) & 1) &&
+                       clock64() - t0 < TIMEOUT_CYCLES) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA
+        if (lane == 0) {
+            int issued = 0;
+            const uint32_t lbo = 128, sbo = 512;
+            for (int idx = 0; idx < total; ++idx) {
+                const int i = idx / nb;
+                const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
+                const int sl = idx % NF, u = idx / NF;
+                if (!mbar_wait(bar(B_F16_FULL + sl), u & 1, abort_flag)) break;
+                if (u > 0 && !mbar_wait(bar(B_TM_EMPTY + sl), (u - 1) & 1, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t fa = sbase + L::O_F16 + sl * F16_SLOT;
+                const uint32_t fbB = fa + F16_A;
+                const uint32_t id = idesc_f16(BM, I.ncols);
+#pragma unroll
+                for (int mat = 0; mat < 2; ++mat) {
+#pragma unroll
+                    for (int k16 = 0; k16 < 2; ++k16) {
+                        mma_f16(tmem + sl * 256 + mat * 128,
+                                sdesc(fa + mat * (BM * 64) + k16 * 256, lbo, sbo),
+                                sdesc(fbB + k16 * 256, lbo, sbo), id, (uint32_t)k16);
+                    }
+                }
+                mma_commit(bar(B_TM_FULL + sl));
+                issued = idx + 1;
+            }
+            if (issued > 0) {  // the last commit covers every MMA issued before it
+                long long t0 = clock64();
+                int last = issued - 1;
+                while (!mbar_try_wait(bar(B_TM_FULL + last % NF), (last / NF) & 1) &&
+                       clock64() - t0 < TIMEOUT_CYCLES) {
+                }
+            }
+        }
+    } else {
+        // --------------------------------------------------------- workers
+        const int wt = threadIdx.x - 64;  // 0..255
+        const int q = warp & 3;           // TMEM lane quarter this warp may access
+        const int h = (warp - 2) >> 2;    // column half
+        const int m = q * 32 + lane;      // weight row (TMEM lane) of this thread
+        float accA[4][16], accB[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) accA[c][j] = accB[c][j] = 0.0f;
+
+        auto convert = [&](int idx) -> bool {
+            const int i = idx / nb;
+            const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
+            const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
+            if (!mbar_wait(bar(B_RAW_FULL + sl), (gs / RS) & 1, abort_flag)) return false;
+            const uint8_t* st = smem + sl * L::STAGE;
+            uint8_t* fa = smem + L::O_F16 + (idx % NF) * F16_SLOT;
+            uint8_t* fbB = fa + F16_A;
+            float* sc = (float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
+            // weights: 256 rows x 32 values of block blk
+            if (WT == MOE_W_Q8_0) {
+#pragma unroll
+                for (int rep = 0; rep < 2; ++rep) {
+                    const int u = wt + rep * 256;
+                    const int R = u >> 1, hh = u & 1;
+                    const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
+                    const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
+                    uint4 o0, o1;
+                    cvt_i8x4(v.x, o0.x, o0.y);
+                    cvt_i8x4(v.y, o0.z, o0.w);
+                    cvt_i8x4(v.z, o1.x, o1.y);
+                    cvt_i8x4(v.w, o1.z, o1.w);
+                    uint8_t* dst = fa + (R >> 7) * (BM * 64);
+                    *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
+                    *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
+                }
+            } else {
+                const int R = wt;
+                const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
+                const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                uint8_t* dst = fa + (R >> 7) * (BM * 64);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t hv[4];
+                    cvt_u4x8(w4[c], hv);
+                    *(uint4*)(dst + f16_off(R & 127, c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                }
+            }
+            // activations: ncols rows x 32 values, units of 16
+            if (wt < 2 * I.ncols) {
+                const int n = wt >> 1, hh = wt & 1;
+                const int ch = (blk * 2 + hh) ^ (n & 7);
+                const uint4 v = *(const uint4*)(st + L::O_X + n * 128 + ch * 16);
+                uint4 o0, o1;
+                if (WT == MOE_W_Q8_0) {
+                    cvt_i8x4(v.x, o0.x, o0.y);
+                    cvt_i8x4(v.y, o0.z, o0.w);
+                    cvt_i8x4(v.z, o1.x, o1.y);
+                    cvt_i8x4(v.w, o1.z, o1.w);
+                } else {
+                    uint32_t a[4], b[4];
+                    cvt_i8x8_interleaved(v.x, v.y, a);
+                    cvt_i8x8_interleaved(v.z, v.w, b);
+                    o0 = make_uint4(a[0], a[1], a[2], a[3]);
+                    o1 = make_uint4(b[0], b[1], b[2], b[3]);
+                }
+                *(uint4*)(fbB + f16_off(n, 2 * hh)) = o0;
+                *(uint4*)(fbB + f16_off(n, 2 * hh + 1)) = o1;
+            }
+            // scales of block blk as fp32: dW[256], mW[256], dX[128], sX[128]
+            {
+                const int R = wt;
+                const int si = GU ? (((R >> 7) * KBS + blk) * BM + (R & 127)) : (blk * 2 * BM + R);
+                const __half* ws = (const __half*)(st + L::O_WS);
+                sc[R] = __half2float(ws[si]);
+                if (WT == MOE_W_Q4_1) sc[2 * BM + R] = __half2float(((const __half*)(st + L::O_WM))[si]);
+                if (R < BN) {
+                    const __half2 xs = ((const __half2*)(st + L::O_XS))[R * KBS + blk];
+                    sc[4 * BM + R] = __low2float(xs);
+                    sc[4 * BM + BN + R] = __high2float(xs);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(bar(B_F16_FULL + idx % NF));
+            if (blk == KBS - 1) mbar_arrive(bar(B_RAW_EMPTY + sl));
+            return true;
+        };
+
+        bool ok = true;
+        for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx) ok = convert(idx);
+        for (int idx = 0; idx < total && ok; ++idx) {
+            const int i = idx / nb, b = idx - i * nb;
+            const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
+            const int sl = idx % NF;
+            if (!mbar_wait(bar(B_TM_FULL + sl), (idx / NF) & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float* sc = (const float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
+            const float dA = sc[m], dB = sc[BM + m];
+            const float mA = WT == MOE_W_Q4_1 ? sc[2 * BM + m] : 0.0f;
+            const float mB = WT == MOE_W_Q4_1 ? sc[3 * BM + m] : 0.0f;
+            const float* dX = sc + 4 * BM;
+            const float* sX = sc + 4 * BM + BN;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + sl * 256;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int col0 = h * 64 + c * 16;
+                if (col0 < I.ncols) {
+                    float pa[16], pb[16];
+                    tmem_ld16(tbase + col0, pa);
+                    tmem_ld16(tbase + 128 + col0, pb);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float dx = dX[col0 + j];
+                        accA[c][j] = __fmaf_rn(__fmul_rn(dA, dx), pa[j], accA[c][j]);
+                        accB[c][j] = __fmaf_rn(__fmul_rn(dB, dx), pb[j], accB[c][j]);
+                        if (WT == MOE_W_Q4_1) {
+                            const float sx = sX[col0 + j];
+                            accA[c][j] = __fmaf_rn(mA, sx, accA[c][j]);
+                            accB[c][j] = __fmaf_rn(mB, sx, accB[c][j]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(B_TM_EMPTY + sl));
+            if (b == nb - 1) {
+                // item complete: write this thread's row for every valid token
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = h * 64 + c * 16 + j;
+                        if (n < I.rows) {
+                            float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
+                            if (GU) {
+                                o[0] = silu_mul(accA[c][j], accB[c][j]);
+                            } else {
+                                o[0] = accA[c][j];
+                                o[BM] = accB[c][j];
+                            }
+                        }
+                        accA[c][j] = accB[c][j] = 0.0f;
+                    }
+                }
+            }
+            if (idx + LOOKAHEAD < total) ok = convert(idx + LOOKAHEAD);
+        }
+    }
+
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) set_error(P.err, MOE_DEV_ERR_TIMEOUT);
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host ----
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+              const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+              CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), (const cuuint64_t*)dims,
+                    (const cuuint64_t*)strides, (const cuuint32_t*)box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int WT, bool GU>
+int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* xq,
+           const uint16_t* xds, int R, int d, int f, float* out, uint8_t* ws, const WsLayout& W,
+           cudaStream_t stream) {
+    using L = Lay<WT>;
+    const RecLayout RL = rec_layout(WT, d, f);
+    const int K = GU ? d : f;          // reduction
+    const int rows = GU ? f : d;       // weight rows per matrix
+    const MatLayout& ML = GU ? RL.gu : RL.dn;
+    const uint8_t* mbase = group_base + (GU ? RL.gate : RL.down);
+    const uint64_t S = (uint64_t)E;    // slots addressable in the group buffer
+    const uint64_t wrow = (uint64_t)K / (WT == MOE_W_Q4_1 ? 2 : 1);
+    CUtensorMap mW, mWs, mWm, mX, mXs;
+    bool ok = true;
+    if (GU) {
+        uint64_t dq[4] = {wrow, (uint64_t)rows, 2, S};
+        uint64_t sq[3] = {wrow, RL.gu.bytes, slot_stride};
+        uint32_t bq[4] = {(uint32_t)L::WROW, BM, 2, 1};
+        ok &= make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, mbase + ML.q, dq, sq, bq,
+                       WT == MOE_W_Q8_0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        uint64_t ds[4] = {(uint64_t)rows, (uint64_t)(K / QK), 2, S};
+        uint64_t ss[3] = {(uint64_t)rows * 2, RL.gu.bytes, slot_stride};
+        uint32_t bs[4] = {BM, KBS, 2, 1};
+        ok &= make_map(&mWs, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, mbase + ML.d, ds, ss, bs,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+        ok &= make_map(&mWm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                       mbase + (WT == MOE_W_Q4_1 ? ML.m : ML.d), ds, ss, bs,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+        uint64_t dq[3] = {wrow, (uint64_t)rows, S};
+        uint64_t sq[2] = {wrow, slot_stride};
+        uint32_t bq[3] = {(uint32_t)L::WROW, 2 * BM, 1};
+        ok &= make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, mbase + ML.q, dq, sq, bq,
+                       WT == MOE_W_Q8_0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        uint64_t ds[3] = {(uint64_t)rows, (uint64_t)(K / QK), S};
+        uint64_t ss[2] = {(uint64_t)rows * 2, slot_stride};
+        uint32_t bs[3] = {2 * BM, KBS, 1};
+        ok &= make_map(&mWs, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, mbase + ML.d, ds, ss, bs,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+        ok &= make_map(&mWm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                       mbase + (WT == MOE_W_Q4_1 ? ML.m : ML.d), ds, ss, bs,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    {
+        uint64_t dx[2] = {(uint64_t)K, (uint64_t)R};
+        uint64_t sx[1] = {(uint64_t)K};
+        uint32_t bx[2] = {128, BN};
+        ok &= make_map(&mX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, xq, dx, sx, bx,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+        uint64_t dd[2] = {(uint64_t)(K / QK), (uint64_t)R};
+        uint64_t sd[1] = {(uint64_t)(K / QK) * 4};
+        uint32_t bd[2] = {KBS, BN};
+        ok &= make_map(&mXs, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, xds, dd, sd, bd,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (!ok) return MOE_ERR_CUDA;
+
+    static int sms = 0;
+    static std::once_flag attr_once;
+    std::call_once(attr_once, [] {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaFuncSetAttribute(mmq_tc_kernel<WT, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::SMEM);
+    });
+    Params P;
+    P.tiles = (const int4*)(ws + W.tiles);
+    P.n_tiles = (const int32_t*)(ws + W.counters) + MMQ_COUNTER_NTILES;
+    P.mt_count = GU ? f / BM : d / (2 * BM);
+    P.nb = K / QK;
+    P.n_out = GU ? f : d;
+    P.out = out;
+    P.err = (uint32_t*)(ws + W.err);
+    long long upper = ((long long)R / BN + E + 1) * P.mt_count;
+    int grid = (int)(upper < sms ? upper : sms);
+    mmq_tc_kernel<WT, GU><<<grid, THREADS, L::SMEM, stream>>>(mW, mWs, mWm, mX, mXs, P);
+    count_launches(1);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace tc
+
+bool mmq_tc_supported(int wtype, bool gateup, int d, int f) {
+    if (wtype != MOE_W_Q8_0 && wtype != MOE_W_Q4_1) return false;
+    if (d % 256 || f % 128) return false;  // whole 128-row weight tiles, 128-wide K stages
+    (void)gateup;
+    return tc::encode_fn() != nullptr;
+}
+
+int launch_mmq_tc(int wtype, bool gateup, const uint8_t* group_base, size_t slot_stride,
+                  const int32_t* active, const int32_t* n_active, const int32_t* offsets, int E,
+                  const int8_t* xq, const uint16_t* xds, int R, int d, int f, float* out,
+                  uint8_t* ws, const WsLayout& W, cudaStream_t stream) {
+    int rc = launch_mmq_tiles(active, n_active, offsets, E, R, tc::BN, ws, W, stream);
+    if (rc != MOE_OK) return rc;
+    if (wtype == MOE_W_Q8_0)
+        return gateup ? tc::launch<MOE_W_Q8_0, true>(group_base, slot_stride, E, xq, xds, R, d, f,
+                                                     out, ws, W, stream)
+                      : tc::launch<MOE_W_Q8_0, false>(group_base, slot_stride, E, xq, xds, R, d, f,
+                                                      out, ws, W, stream);
+    return gateup ? tc::launch<MOE_W_Q4_1, true>(group_base, slot_stride, E, xq, xds, R, d, f, out,
+                                                 ws, W, stream)
+                  : tc::launch<MOE_W_Q4_1, false>(group_base, slot_stride, E, xq, xds, R, d, f, out,
+                                                  ws, W, stream);
 }
 
 }  // namespace moe

@@ -262,6 +262,28 @@ def test_mmq_down(name):
     assert err.max() <= 1e-5, err.max()
 
 
+@pytest.mark.parametrize("stage", ["gateup", "down"])
+@pytest.mark.parametrize("name", [mw.TINY.name, mw.T600.name, mw.T2048.name, mw.T8192.name])
+def test_mmq_tensor_cores_match_cuda_cores(name, stage, monkeypatch):
+    """The tcgen05 kernel forms each block's integer dot exactly and scales it in
+    the same fp32 order as the dp4a kernel, so the two agree bit for bit."""
+    wl = H.workload(name)
+    cfg = wl.cfg
+    o = oracle.build_slot_map(wl.ids, cfg.E)
+    R = int(o["offsets"][cfg.E])
+    if stage == "gateup":
+        xq, xds = oracle.quantize_scatter_q8_1(wl.x, o["slot"], cfg.K, R)
+    else:
+        hid = mw.normal_f32(cfg.seed, 9, R * cfg.f, scale=0.05).reshape(R, cfg.f)
+        xq, xds = oracle.requant_hidden_q8_1(hid)
+    tc = _mmq_gpu(stage, wl, o, xq, xds)
+    monkeypatch.setenv("MOE_MMQ_PATH", "simt")
+    simt = _mmq_gpu(stage, wl, o, xq, xds)
+    assert np.isfinite(tc).all()
+    diff = np.nonzero(tc.view(np.uint32) != simt.view(np.uint32))
+    assert diff[0].size == 0, (diff[0][:8], diff[1][:8], tc[diff][:8], simt[diff][:8])
+
+
 @pytest.mark.parametrize("name", ALL)
 def test_requant_hidden(name):
     cfg = mw.CONFIGS[name]
