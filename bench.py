@@ -403,11 +403,18 @@ def run_stage(args):
         return _time_stage(args, cfg, lambda: m.moe_quantize_scatter_q8_1(x, slot, K, R, q, ds),
                            ws, int(na.item()), 0)
     wl = mw.make_workload(cfg)
-    arena = torch.from_numpy(wl.arena).to(dev)
+    # only the routed experts' records go to the device (ids renumbered to them),
+    # so a profiler capture holds ~1-2 GB instead of the whole expert arena
+    used = np.unique(wl.ids)
+    st = wl.arena_stride
+    arena_h = np.concatenate([wl.arena[e * st:(e + 1) * st] for e in used])
+    ids_h = np.searchsorted(used, wl.ids).astype(np.int32)
+    E = len(used)
+    arena = torch.from_numpy(arena_h).to(dev)
     x = torch.from_numpy(wl.x).to(dev)
-    ids = torch.from_numpy(wl.ids).to(dev)
+    ids = torch.from_numpy(ids_h).to(dev)
     w = torch.from_numpy(wl.w).to(dev)
-    L = m.MoeLayer(cfg.wtype, E, d, f, K, T, arena, wl.rec_bytes, wl.arena_stride, dev)
+    L = m.MoeLayer(cfg.wtype, E, d, f, K, T, arena, wl.rec_bytes, st, dev)
     L.forward(x, ids, w)
     calls = {
         "quantize_scatter": lambda: m.moe_quantize_scatter_q8_1(x, L.slot, K, R, L.q, L.ds),

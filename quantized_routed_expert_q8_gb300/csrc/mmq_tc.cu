@@ -13,20 +13,25 @@
 // integer.  The per-block fp32 scaling then runs on the CUDA cores in the same
 // order as the scalar definition: acc = fma(dW*dx, I_b, acc) (+ fma(mW, sx, acc)).
 //
-// One persistent CTA per SM (static round-robin over the device-built,
-// longest-first work list).  A work item is 128 tokens of one expert times two
-// 128-row weight blocks (gate and up rows j0..j0+127 for stage 4; down rows
-// i0..i0+255 for stage 6).  Warp roles:
-//   warp 0      TMA producer: raw int8 / 4-bit tiles and fp16 scales, 4 blocks a stage
-//   warp 1      MMA issuer: per 32-block, 2 x (M=128, N<=128, K=16) per matrix into
-//               one of two TMEM buffers, committed to an mbarrier
-//   warps 2-9   workers: for block b, read the partials out of TMEM, scale and
-//               accumulate in registers; then convert block b+2's raw tiles into
-//               the fp16 operand layout for the MMA.
+// One persistent CTA of 8 warps per SM (static round-robin over the
+// device-built, longest-first work list).  A work item is 128 tokens of one
+// expert times two 128-row weight blocks (gate and up rows j0..j0+127 for
+// stage 4; down rows i0..i0+255 for stage 6).  Every warp is a worker: for
+// 32-block b it reads its quarter of the TMEM lanes (its weight rows) for its
+// half of the columns (tokens), scales and accumulates in registers (128 fp32
+// per thread), then converts block b+2's raw tiles into the fp16 operand
+// layout.  Two threads carry extra duties: thread 0 issues the TMA loads of
+// raw int8 / 4-bit tiles and fp16 scales (4 blocks a stage, never blocking),
+// thread 32 issues block b+1's MMAs -- 2 x (M=128, N<=128, K=16) per matrix --
+// into the TMEM buffer the workers are not reading, committed to an mbarrier.
+// (The register file is split over the four SM sub-partitions, so 8 warps of
+// up to 255 registers fit where 10 warps of 200 would not.)
 // Every wait is bounded: on timeout the kernel sets MOE_DEV_ERR_TIMEOUT, drains
 // what it started and exits.
 #include <cudaTypedefs.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "mmq.cuh"
@@ -40,8 +45,7 @@ constexpr int KBS = 4;       // 32-blocks per raw stage
 constexpr int RS = 3;        // raw stages
 constexpr int NF = 2;        // fp16 operand slots = TMEM partial buffers
 constexpr int NSC = 4;       // scale ring slots
-constexpr int NWORK = 8;     // worker warps
-constexpr int THREADS = 32 * (2 + NWORK);
+constexpr int THREADS = 256; // 8 warps, 2 per SM sub-partition
 constexpr int LOOKAHEAD = 2; // blocks converted ahead of the epilogue
 constexpr long long TIMEOUT_CYCLES = 1LL << 32;
 
@@ -187,8 +191,9 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 16 consecutive TMEM columns of this thread's lane; the values are valid only
+// after tmem_wait16 on the same registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
         "%12, %13, %14, %15}, [%16];"
@@ -196,12 +201,39 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// Wait for this thread's outstanding TMEM loads.  The loaded registers pass
+// through the statement so no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait32(uint32_t (&a)[16], uint32_t (&b)[16]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
+          "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]),
+          "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]),
+          "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]),
+          "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
+        :
+        : "memory");
+}
+
+// Packed fp32 pairs (two IEEE round-to-nearest operations per instruction).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -282,7 +314,7 @@ __device__ __forceinline__ Item load_item(const Params& P, int it) {
 }
 
 template <int WT, bool GU>
-__global__ void __maxnreg__(200)  // 320 threads x 200 registers fit one CTA per SM
+__global__ void __launch_bounds__(THREADS, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mWs,
                   const __grid_constant__ CUtensorMap mWm, const __grid_constant__ CUtensorMap mX,
                   const __grid_constant__ CUtensorMap mXs, const Params P) {
@@ -294,7 +326,6 @@ __global__ void __maxnreg__(200)  // 320 threads x 200 registers fit one CTA per
     uint32_t* tmem_slot = (uint32_t*)(smem + L::O_BAR + L::N_BARS * 8);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
-    // barrier indices
     const int B_RAW_FULL = 0, B_RAW_EMPTY = RS, B_F16_FULL = 2 * RS, B_TM_FULL = 2 * RS + NF,
               B_TM_EMPTY = 2 * RS + 2 * NF;
 
@@ -304,17 +335,20 @@ __global__ void __maxnreg__(200)  // 320 threads x 200 registers fit one CTA per
     const int nb = P.nb;
     const int spi = nb / KBS;  // raw stages per item
     const int total = my_items * nb;
+    const int total_stages = my_items * spi;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool is_producer = threadIdx.x == 0;
+    const bool is_mma = threadIdx.x == 32;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
             mbar_init(bar(B_RAW_FULL + i), 1);
-            mbar_init(bar(B_RAW_EMPTY + i), NWORK * 32);
+            mbar_init(bar(B_RAW_EMPTY + i), THREADS);
         }
         for (int i = 0; i < NF; ++i) {
-            mbar_init(bar(B_F16_FULL + i), NWORK * 32);
+            mbar_init(bar(B_F16_FULL + i), THREADS);
             mbar_init(bar(B_TM_FULL + i), 1);
-            mbar_init(bar(B_TM_EMPTY + i), NWORK * 32);
+            mbar_init(bar(B_TM_EMPTY + i), THREADS);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -330,230 +364,283 @@ __global__ void __maxnreg__(200)  // 320 threads x 200 registers fit one CTA per
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int gs = 0; gs < my_items * spi; ++gs) {
-                const int i = gs / spi, s = gs - i * spi;
-                const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
-                const int sl = gs % RS, u = gs / RS;
-                if (u > 0 && !mbar_wait(bar(B_RAW_EMPTY + sl), (u - 1) & 1, abort_flag)) break;
-                const uint32_t st = sbase + sl * L::STAGE;
-                const uint32_t fb = bar(B_RAW_FULL + sl);
-                mbar_expect_tx(fb, L::TX);
-                if (GU) {
-                    tma_4d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, 0, I.p);
-                    tma_4d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, 0, I.p);
-                    if (WT == MOE_W_Q4_1) tma_4d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, 0, I.p);
-                } else {
-                    tma_3d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, I.p);
-                    tma_3d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, I.p);
-                    if (WT == MOE_W_Q4_1) tma_3d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, I.p);
-                }
-                tma_2d(&mX, fb, st + L::O_X, s * 128, I.r0);
-                tma_2d(&mXs, fb, st + L::O_XS, s * KBS, I.r0);
-                issued = gs + 1;
-            }
-            // drain: every stage issued must have landed before the CTA may exit
-            for (int gs = (issued > RS ? issued - RS : 0); gs < issued; ++gs) {
-                long long t0 = clock64();
-                while (!mbar_try_wait(bar(B_RAW_FULL + gs % RS), (gs / RS) & 1) &&
-                       clock64() - t0 < TIMEOUT_CYCLES) {
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------- MMA
-        if (lane == 0) {
-            int issued = 0;
-            const uint32_t lbo = 128, sbo = 512;
-            for (int idx = 0; idx < total; ++idx) {
-                const int i = idx / nb;
-                const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
-                const int sl = idx % NF, u = idx / NF;
-                if (!mbar_wait(bar(B_F16_FULL + sl), u & 1, abort_flag)) break;
-                if (u > 0 && !mbar_wait(bar(B_TM_EMPTY + sl), (u - 1) & 1, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t fa = sbase + L::O_F16 + sl * F16_SLOT;
-                const uint32_t fbB = fa + F16_A;
-                const uint32_t id = idesc_f16(BM, I.ncols);
-#pragma unroll
-                for (int mat = 0; mat < 2; ++mat) {
-#pragma unroll
-                    for (int k16 = 0; k16 < 2; ++k16) {
-                        mma_f16(tmem + sl * 256 + mat * 128,
-                                sdesc(fa + mat * (BM * 64) + k16 * 256, lbo, sbo),
-                                sdesc(fbB + k16 * 256, lbo, sbo), id, (uint32_t)k16);
-                    }
-                }
-                mma_commit(bar(B_TM_FULL + sl));
-                issued = idx + 1;
-            }
-            if (issued > 0) {  // the last commit covers every MMA issued before it
-                long long t0 = clock64();
-                int last = issued - 1;
-                while (!mbar_try_wait(bar(B_TM_FULL + last % NF), (last / NF) & 1) &&
-                       clock64() - t0 < TIMEOUT_CYCLES) {
-                }
-            }
-        }
-    } else {
-        // --------------------------------------------------------- workers
-        const int wt = threadIdx.x - 64;  // 0..255
-        const int q = warp & 3;           // TMEM lane quarter this warp may access
-        const int h = (warp - 2) >> 2;    // column half
-        const int m = q * 32 + lane;      // weight row (TMEM lane) of this thread
-        float accA[4][16], accB[4][16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int j = 0; j < 16; ++j) accA[c][j] = accB[c][j] = 0.0f;
-
-        auto convert = [&](int idx) -> bool {
-            const int i = idx / nb;
+    // ---- producer duty (thread 0): issue every raw stage whose slot is free.
+    // Never blocks; called at each step and from inside thread 0's waits.
+    int next_stage = 0;
+    auto produce = [&]() {
+        while (next_stage < total_stages) {
+            const int gs = next_stage, sl = gs % RS, u = gs / RS;
+            if (u > 0 && !mbar_try_wait(bar(B_RAW_EMPTY + sl), (u - 1) & 1)) return;
+            const int i = gs / spi, s = gs - i * spi;
             const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
-            const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
-            if (!mbar_wait(bar(B_RAW_FULL + sl), (gs / RS) & 1, abort_flag)) return false;
-            const uint8_t* st = smem + sl * L::STAGE;
-            uint8_t* fa = smem + L::O_F16 + (idx % NF) * F16_SLOT;
-            uint8_t* fbB = fa + F16_A;
-            float* sc = (float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
-            // weights: 256 rows x 32 values of block blk
-            if (WT == MOE_W_Q8_0) {
-#pragma unroll
-                for (int rep = 0; rep < 2; ++rep) {
-                    const int u = wt + rep * 256;
-                    const int R = u >> 1, hh = u & 1;
-                    const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
-                    const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
-                    uint4 o0, o1;
-                    cvt_i8x4(v.x, o0.x, o0.y);
-                    cvt_i8x4(v.y, o0.z, o0.w);
-                    cvt_i8x4(v.z, o1.x, o1.y);
-                    cvt_i8x4(v.w, o1.z, o1.w);
-                    uint8_t* dst = fa + (R >> 7) * (BM * 64);
-                    *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
-                    *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
-                }
+            const uint32_t st = sbase + sl * L::STAGE;
+            const uint32_t fb = bar(B_RAW_FULL + sl);
+            mbar_expect_tx(fb, L::TX);
+            if (GU) {
+                tma_4d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, 0, I.p);
+                tma_4d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, 0, I.p);
+                if (WT == MOE_W_Q4_1) tma_4d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, 0, I.p);
             } else {
-                const int R = wt;
-                const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
-                const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                uint8_t* dst = fa + (R >> 7) * (BM * 64);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t hv[4];
-                    cvt_u4x8(w4[c], hv);
-                    *(uint4*)(dst + f16_off(R & 127, c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                }
+                tma_3d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, I.p);
+                tma_3d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, I.p);
+                if (WT == MOE_W_Q4_1) tma_3d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, I.p);
             }
-            // activations: ncols rows x 32 values, units of 16
-            if (wt < 2 * I.ncols) {
-                const int n = wt >> 1, hh = wt & 1;
-                const int ch = (blk * 2 + hh) ^ (n & 7);
-                const uint4 v = *(const uint4*)(st + L::O_X + n * 128 + ch * 16);
-                uint4 o0, o1;
-                if (WT == MOE_W_Q8_0) {
-                    cvt_i8x4(v.x, o0.x, o0.y);
-                    cvt_i8x4(v.y, o0.z, o0.w);
-                    cvt_i8x4(v.z, o1.x, o1.y);
-                    cvt_i8x4(v.w, o1.z, o1.w);
-                } else {
-                    uint32_t a[4], b[4];
-                    cvt_i8x8_interleaved(v.x, v.y, a);
-                    cvt_i8x8_interleaved(v.z, v.w, b);
-                    o0 = make_uint4(a[0], a[1], a[2], a[3]);
-                    o1 = make_uint4(b[0], b[1], b[2], b[3]);
-                }
-                *(uint4*)(fbB + f16_off(n, 2 * hh)) = o0;
-                *(uint4*)(fbB + f16_off(n, 2 * hh + 1)) = o1;
+            tma_2d(&mX, fb, st + L::O_X, s * 128, I.r0);
+            tma_2d(&mXs, fb, st + L::O_XS, s * KBS, I.r0);
+            ++next_stage;
+        }
+    };
+    // bounded wait; thread 0 keeps producing while it waits
+    auto waitp = [&](uint32_t b, uint32_t parity) -> bool {
+        if (mbar_try_wait(b, parity)) return true;
+        long long t0 = clock64();
+        while (true) {
+            if (is_producer) produce();
+            if (mbar_try_wait(b, parity)) return true;
+            if (*abort_flag) return false;
+            if (clock64() - t0 > TIMEOUT_CYCLES) {
+                *abort_flag = 1;
+                return false;
             }
-            // scales of block blk as fp32: dW[256], mW[256], dX[128], sX[128]
-            {
-                const int R = wt;
-                const int si = GU ? (((R >> 7) * KBS + blk) * BM + (R & 127)) : (blk * 2 * BM + R);
-                const __half* ws = (const __half*)(st + L::O_WS);
-                sc[R] = __half2float(ws[si]);
-                if (WT == MOE_W_Q4_1) sc[2 * BM + R] = __half2float(((const __half*)(st + L::O_WM))[si]);
-                if (R < BN) {
-                    const __half2 xs = ((const __half2*)(st + L::O_XS))[R * KBS + blk];
-                    sc[4 * BM + R] = __low2float(xs);
-                    sc[4 * BM + BN + R] = __high2float(xs);
-                }
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(bar(B_F16_FULL + idx % NF));
-            if (blk == KBS - 1) mbar_arrive(bar(B_RAW_EMPTY + sl));
-            return true;
-        };
+        }
+    };
 
-        bool ok = true;
-        for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx) ok = convert(idx);
-        for (int idx = 0; idx < total && ok; ++idx) {
-            const int i = idx / nb, b = idx - i * nb;
-            const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
-            const int sl = idx % NF;
-            if (!mbar_wait(bar(B_TM_FULL + sl), (idx / NF) & 1, abort_flag)) {
-                ok = false;
-                break;
+    // ---- MMA duty (thread 32): block idx's products into TMEM buffer idx % 2.
+    int mma_issued = 0;
+    auto issue_mma = [&](int idx) -> bool {
+        const Item I = load_item<GU>(P, (int)blockIdx.x + (idx / nb) * (int)gridDim.x);
+        const int sl = idx % NF, u = idx / NF;
+        if (!waitp(bar(B_F16_FULL + sl), u & 1)) return false;
+        if (u > 0 && !waitp(bar(B_TM_EMPTY + sl), (u - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t fa = sbase + L::O_F16 + sl * F16_SLOT;
+        const uint32_t fbB = fa + F16_A;
+        const uint32_t id = idesc_f16(BM, I.ncols);
+#pragma unroll
+        for (int mat = 0; mat < 2; ++mat) {
+#pragma unroll
+            for (int k16 = 0; k16 < 2; ++k16) {
+                mma_f16(tmem + sl * 256 + mat * 128, sdesc(fa + mat * (BM * 64) + k16 * 256, 128, 512),
+                        sdesc(fbB + k16 * 256, 128, 512), id, (uint32_t)k16);
             }
-            tc_fence_after();
-            const float* sc = (const float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
-            const float dA = sc[m], dB = sc[BM + m];
-            const float mA = WT == MOE_W_Q4_1 ? sc[2 * BM + m] : 0.0f;
-            const float mB = WT == MOE_W_Q4_1 ? sc[3 * BM + m] : 0.0f;
-            const float* dX = sc + 4 * BM;
-            const float* sX = sc + 4 * BM + BN;
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + sl * 256;
+        }
+        mma_commit(bar(B_TM_FULL + sl));
+        mma_issued = idx + 1;
+        return true;
+    };
+
+    // ---- worker duty (all threads)
+    const int wt = threadIdx.x;     // 0..255
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int h = warp >> 2;        // column half
+    const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
+    float accA[4][16], accB[4][16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) accA[c][j] = accB[c][j] = 0.0f;
+
+    auto convert = [&](int idx) -> bool {
+        const int i = idx / nb;
+        const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
+        const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
+        if (!waitp(bar(B_RAW_FULL + sl), (gs / RS) & 1)) return false;
+        const uint8_t* st = smem + sl * L::STAGE;
+        uint8_t* fa = smem + L::O_F16 + (idx % NF) * F16_SLOT;
+        uint8_t* fbB = fa + F16_A;
+        float* sc = (float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
+        // weights: 256 rows x 32 values of block blk
+        if (WT == MOE_W_Q8_0) {
+#pragma unroll
+            for (int rep = 0; rep < 2; ++rep) {
+                const int u = wt + rep * 256;
+                const int R = u >> 1, hh = u & 1;
+                const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
+                const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
+                uint4 o0, o1;
+                cvt_i8x4(v.x, o0.x, o0.y);
+                cvt_i8x4(v.y, o0.z, o0.w);
+                cvt_i8x4(v.z, o1.x, o1.y);
+                cvt_i8x4(v.w, o1.z, o1.w);
+                uint8_t* dst = fa + (R >> 7) * (BM * 64);
+                *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
+                *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
+            }
+        } else {
+            const int R = wt;
+            const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
+            const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint8_t* dst = fa + (R >> 7) * (BM * 64);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int col0 = h * 64 + c * 16;
-                if (col0 < I.ncols) {
-                    float pa[16], pb[16];
-                    tmem_ld16(tbase + col0, pa);
-                    tmem_ld16(tbase + 128 + col0, pb);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float dx = dX[col0 + j];
-                        accA[c][j] = __fmaf_rn(__fmul_rn(dA, dx), pa[j], accA[c][j]);
-                        accB[c][j] = __fmaf_rn(__fmul_rn(dB, dx), pb[j], accB[c][j]);
-                        if (WT == MOE_W_Q4_1) {
-                            const float sx = sX[col0 + j];
-                            accA[c][j] = __fmaf_rn(mA, sx, accA[c][j]);
-                            accB[c][j] = __fmaf_rn(mB, sx, accB[c][j]);
-                        }
-                    }
-                }
+                uint32_t hv[4];
+                cvt_u4x8(w4[c], hv);
+                *(uint4*)(dst + f16_off(R & 127, c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             }
-            tc_fence_before();
-            mbar_arrive(bar(B_TM_EMPTY + sl));
-            if (b == nb - 1) {
-                // item complete: write this thread's row for every valid token
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int n = h * 64 + c * 16 + j;
-                        if (n < I.rows) {
-                            float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
-                            if (GU) {
-                                o[0] = silu_mul(accA[c][j], accB[c][j]);
-                            } else {
-                                o[0] = accA[c][j];
-                                o[BM] = accB[c][j];
-                            }
-                        }
-                        accA[c][j] = accB[c][j] = 0.0f;
-                    }
-                }
-            }
-            if (idx + LOOKAHEAD < total) ok = convert(idx + LOOKAHEAD);
         }
+        // activations: ncols rows x 32 values, units of 16
+        if (wt < 2 * I.ncols) {
+            const int n = wt >> 1, hh = wt & 1;
+            const int ch = (blk * 2 + hh) ^ (n & 7);
+            const uint4 v = *(const uint4*)(st + L::O_X + n * 128 + ch * 16);
+            uint4 o0, o1;
+            if (WT == MOE_W_Q8_0) {
+                cvt_i8x4(v.x, o0.x, o0.y);
+                cvt_i8x4(v.y, o0.z, o0.w);
+                cvt_i8x4(v.z, o1.x, o1.y);
+                cvt_i8x4(v.w, o1.z, o1.w);
+            } else {
+                uint32_t a[4], b[4];
+                cvt_i8x8_interleaved(v.x, v.y, a);
+                cvt_i8x8_interleaved(v.z, v.w, b);
+                o0 = make_uint4(a[0], a[1], a[2], a[3]);
+                o1 = make_uint4(b[0], b[1], b[2], b[3]);
+            }
+            *(uint4*)(fbB + f16_off(n, 2 * hh)) = o0;
+            *(uint4*)(fbB + f16_off(n, 2 * hh + 1)) = o1;
+        }
+        // scales of block blk as fp32: dW[256], mW[256], dX[128], sX[128]
+        {
+            const int R = wt;
+            const int si = GU ? (((R >> 7) * KBS + blk) * BM + (R & 127)) : (blk * 2 * BM + R);
+            sc[R] = __half2float(((const __half*)(st + L::O_WS))[si]);
+            if (WT == MOE_W_Q4_1) sc[2 * BM + R] = __half2float(((const __half*)(st + L::O_WM))[si]);
+            if (R < BN) {
+                const __half2 xs = ((const __half2*)(st + L::O_XS))[R * KBS + blk];
+                sc[4 * BM + R] = __low2float(xs);
+                sc[4 * BM + BN + R] = __high2float(xs);
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(bar(B_F16_FULL + idx % NF));
+        if (blk == KBS - 1) mbar_arrive(bar(B_RAW_EMPTY + sl));
+        return true;
+    };
+
+    auto epilogue = [&](int idx) -> bool {
+        const int i = idx / nb, b = idx - i * nb;
+        const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
+        const int sl = idx % NF;
+        // warp-uniform decision: the TMEM loads below are warp-collective
+        if (!__all_sync(0xffffffffu, waitp(bar(B_TM_FULL + sl), (idx / NF) & 1))) return false;
+        tc_fence_after();
+        const float* sc = (const float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
+        const float dA = sc[m], dB = sc[BM + m];
+        const float mA = WT == MOE_W_Q4_1 ? sc[2 * BM + m] : 0.0f;
+        const float mB = WT == MOE_W_Q4_1 ? sc[3 * BM + m] : 0.0f;
+        const float* dX = sc + 4 * BM;
+        const float* sX = sc + 4 * BM + BN;
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + sl * 256;
+        const int nch = min(4, max(0, (I.ncols - h * 64) / 16));  // active 16-column chunks
+        // software pipeline: chunk c+1's TMEM loads are in flight while chunk c is scaled
+        uint32_t ra[2][16], rb[2][16];
+        if (nch > 0) {
+            tmem_ld16(tbase + h * 64, ra[0]);
+            tmem_ld16(tbase + 128 + h * 64, rb[0]);
+            tmem_wait32(ra[0], rb[0]);
+        }
+        const float2 dA2 = make_float2(dA, dA), dB2 = make_float2(dB, dB);
+        const float2 mA2 = make_float2(mA, mA), mB2 = make_float2(mB, mB);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (c < nch) {
+                const int cur = c & 1, nxt = cur ^ 1;
+                const int col0 = h * 64 + c * 16;
+                if (c + 1 < nch) {
+                    tmem_ld16(tbase + col0 + 16, ra[nxt]);
+                    tmem_ld16(tbase + 128 + col0 + 16, rb[nxt]);
+                }
+                const float4* dx4 = reinterpret_cast<const float4*>(dX + col0);
+                const float4* sx4 = reinterpret_cast<const float4*>(sX + col0);
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    const float4 dx = dx4[j4];
+                    const float2 dlo = make_float2(dx.x, dx.y), dhi = make_float2(dx.z, dx.w);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int j = j4 * 4 + e * 2;
+                        const float2 d2 = e ? dhi : dlo;
+                        const float2 pa = make_float2(__uint_as_float(ra[cur][j]),
+                                                      __uint_as_float(ra[cur][j + 1]));
+                        const float2 pb = make_float2(__uint_as_float(rb[cur][j]),
+                                                      __uint_as_float(rb[cur][j + 1]));
+                        float2 xa = make_float2(accA[c][j], accA[c][j + 1]);
+                        float2 xb = make_float2(accB[c][j], accB[c][j + 1]);
+                        xa = fma2(mul2(dA2, d2), pa, xa);
+                        xb = fma2(mul2(dB2, d2), pb, xb);
+                        if (WT == MOE_W_Q4_1) {
+                            const float4 sx = sx4[j4];
+                            const float2 s2 = e ? make_float2(sx.z, sx.w) : make_float2(sx.x, sx.y);
+                            xa = fma2(mA2, s2, xa);
+                            xb = fma2(mB2, s2, xb);
+                        }
+                        accA[c][j] = xa.x;
+                        accA[c][j + 1] = xa.y;
+                        accB[c][j] = xb.x;
+                        accB[c][j + 1] = xb.y;
+                    }
+                }
+                if (c + 1 < nch) tmem_wait32(ra[nxt], rb[nxt]);
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_TM_EMPTY + sl));
+        if (b == nb - 1) {
+            // item complete: write this thread's row for every valid token
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int n = h * 64 + c * 16 + j;
+                    if (n < I.rows) {
+                        float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
+                        if (GU) {
+                            o[0] = silu_mul(accA[c][j], accB[c][j]);
+                        } else {
+                            o[0] = accA[c][j];
+                            o[BM] = accB[c][j];
+                        }
+                    }
+                    accA[c][j] = accB[c][j] = 0.0f;
+                }
+            }
+        }
+        return true;
+    };
+
+    // Every lane runs every step, and each step's continue/stop decision is
+    // warp-uniform (__all_sync), so the warp-collective TMEM loads never see a
+    // diverged warp; a failed MMA issue only raises the abort flag, which the
+    // next waits observe.
+    bool ok = true;
+    if (is_producer) produce();
+    for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx)
+        ok = __all_sync(0xffffffffu, convert(idx));
+    if (ok && is_mma) issue_mma(0);
+    for (int idx = 0; idx < total && ok; ++idx) {
+        if (is_producer) produce();
+        if (is_mma && idx + 1 < total) issue_mma(idx + 1);
+        ok = epilogue(idx);
+        if (ok && idx + LOOKAHEAD < total) ok = __all_sync(0xffffffffu, convert(idx + LOOKAHEAD));
     }
 
+    // drain what this CTA started before it may exit (only waits on the abort path)
+    if (is_producer) {
+        for (int gs = (next_stage > RS ? next_stage - RS : 0); gs < next_stage; ++gs) {
+            long long t0 = clock64();
+            while (!mbar_try_wait(bar(B_RAW_FULL + gs % RS), (gs / RS) & 1) &&
+                   clock64() - t0 < TIMEOUT_CYCLES) {
+            }
+        }
+    }
+    if (is_mma && mma_issued > 0) {
+        const int last = mma_issued - 1;
+        long long t0 = clock64();
+        while (!mbar_try_wait(bar(B_TM_FULL + last % NF), (last / NF) & 1) &&
+               clock64() - t0 < TIMEOUT_CYCLES) {
+        }
+    }
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) set_error(P.err, MOE_DEV_ERR_TIMEOUT);
     if (warp == 0) {
@@ -580,9 +667,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+bool debug() {
+    static const bool on = std::getenv("MOE_DEBUG") != nullptr;
+    return on;
+}
+
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
               const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
-              CUtensorMapSwizzle sw) {
+              CUtensorMapSwizzle sw, const char* what) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
@@ -590,6 +682,17 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
                     (const cuuint64_t*)strides, (const cuuint32_t*)box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS && debug()) {
+        std::fprintf(stderr, "moe_q8: tensor map %s rejected (CUresult %d), rank %d base %p dims",
+                     what, (int)r, rank, base);
+        for (int i = 0; i < rank; ++i) std::fprintf(stderr, " %llu", (unsigned long long)dims[i]);
+        std::fprintf(stderr, " strides");
+        for (int i = 0; i + 1 < rank; ++i)
+            std::fprintf(stderr, " %llu", (unsigned long long)strides[i]);
+        std::fprintf(stderr, " box");
+        for (int i = 0; i < rank; ++i) std::fprintf(stderr, " %u", box[i]);
+        std::fprintf(stderr, "\n");
+    }
     return r == CUDA_SUCCESS;
 }
 
@@ -612,41 +715,41 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
         uint64_t sq[3] = {wrow, RL.gu.bytes, slot_stride};
         uint32_t bq[4] = {(uint32_t)L::WROW, BM, 2, 1};
         ok &= make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, mbase + ML.q, dq, sq, bq,
-                       WT == MOE_W_Q8_0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                       WT == MOE_W_Q8_0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "W (gate/up)");
         uint64_t ds[4] = {(uint64_t)rows, (uint64_t)(K / QK), 2, S};
         uint64_t ss[3] = {(uint64_t)rows * 2, RL.gu.bytes, slot_stride};
         uint32_t bs[4] = {BM, KBS, 2, 1};
         ok &= make_map(&mWs, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, mbase + ML.d, ds, ss, bs,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+                       CU_TENSOR_MAP_SWIZZLE_NONE, "W scales (gate/up)");
         ok &= make_map(&mWm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
                        mbase + (WT == MOE_W_Q4_1 ? ML.m : ML.d), ds, ss, bs,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+                       CU_TENSOR_MAP_SWIZZLE_NONE, "W mins (gate/up)");
     } else {
         uint64_t dq[3] = {wrow, (uint64_t)rows, S};
         uint64_t sq[2] = {wrow, slot_stride};
         uint32_t bq[3] = {(uint32_t)L::WROW, 2 * BM, 1};
         ok &= make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, mbase + ML.q, dq, sq, bq,
-                       WT == MOE_W_Q8_0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                       WT == MOE_W_Q8_0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "W (down)");
         uint64_t ds[3] = {(uint64_t)rows, (uint64_t)(K / QK), S};
         uint64_t ss[2] = {(uint64_t)rows * 2, slot_stride};
         uint32_t bs[3] = {2 * BM, KBS, 1};
         ok &= make_map(&mWs, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, mbase + ML.d, ds, ss, bs,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+                       CU_TENSOR_MAP_SWIZZLE_NONE, "W scales (down)");
         ok &= make_map(&mWm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                        mbase + (WT == MOE_W_Q4_1 ? ML.m : ML.d), ds, ss, bs,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+                       CU_TENSOR_MAP_SWIZZLE_NONE, "W mins (down)");
     }
     {
         uint64_t dx[2] = {(uint64_t)K, (uint64_t)R};
         uint64_t sx[1] = {(uint64_t)K};
         uint32_t bx[2] = {128, BN};
         ok &= make_map(&mX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, xq, dx, sx, bx,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
+                       CU_TENSOR_MAP_SWIZZLE_128B, "X");
         uint64_t dd[2] = {(uint64_t)(K / QK), (uint64_t)R};
         uint64_t sd[1] = {(uint64_t)(K / QK) * 4};
         uint32_t bd[2] = {KBS, BN};
         ok &= make_map(&mXs, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, xds, dd, sd, bd,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+                       CU_TENSOR_MAP_SWIZZLE_NONE, "X scales");
     }
     if (!ok) return MOE_ERR_CUDA;
 
@@ -656,8 +759,10 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaFuncSetAttribute(mmq_tc_kernel<WT, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel<WT, GU>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+        if (e != cudaSuccess && debug())
+            std::fprintf(stderr, "moe_q8: smem attribute failed: %s\n", cudaGetErrorString(e));
     });
     Params P;
     P.tiles = (const int4*)(ws + W.tiles);
@@ -671,7 +776,11 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     int grid = (int)(upper < sms ? upper : sms);
     mmq_tc_kernel<WT, GU><<<grid, THREADS, L::SMEM, stream>>>(mW, mWs, mWm, mX, mXs, P);
     count_launches(1);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess && debug())
+        std::fprintf(stderr, "moe_q8: mmq_tc launch failed: %s (grid %d, smem %d)\n",
+                     cudaGetErrorString(e), grid, L::SMEM);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace tc
