@@ -47,6 +47,7 @@ constexpr int NF = 2;        // fp16 operand slots = TMEM partial buffers
 constexpr int NSC = 4;       // scale ring slots
 constexpr int THREADS = 256; // 8 warps, 2 per SM sub-partition
 constexpr int LOOKAHEAD = 2; // blocks converted ahead of the epilogue
+constexpr int ITEM_RING = 8; // work items kept in shared memory (written by the producer)
 constexpr long long TIMEOUT_CYCLES = 1LL << 32;
 
 constexpr int F16_A = 2 * BM * 64;  // two 128-row matrices x 32 fp16
@@ -75,7 +76,8 @@ struct Lay {
     static constexpr int O_SC = O_F16 + NF * F16_SLOT;
     static constexpr int O_BAR = O_SC + NSC * SC_SLOT;
     static constexpr int N_BARS = 2 * RS + 3 * NF;
-    static constexpr int SMEM = O_BAR + N_BARS * 8 + 16 + 1024;  // + alignment slack
+    static constexpr int O_ITEMS = cround(O_BAR + N_BARS * 8 + 16, 16);
+    static constexpr int SMEM = O_ITEMS + ITEM_RING * 16 + 1024;  // + alignment slack
 };
 
 // ------------------------------------------------------------------ PTX ----
@@ -108,6 +110,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// As mbar_try_wait, but the thread may sleep in hardware (up to ~20 us) until
+// the phase completes instead of spinning on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
         : "memory");
     return ok != 0;
 }
@@ -217,22 +232,27 @@ __device__ __forceinline__ void tmem_wait32(uint32_t (&a)[16], uint32_t (&b)[16]
         : "memory");
 }
 
-// Packed fp32 pairs (two IEEE round-to-nearest operations per instruction).
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+// Packed fp32 pairs in 64-bit registers (two IEEE round-to-nearest operations
+// per instruction); element 0 in the low half.
+__device__ __forceinline__ uint64_t pk2(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
     return d;
 }
-
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+    uint32_t a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(a), "=r"(b) : "l"(v));
+    lo = __uint_as_float(a);
+    hi = __uint_as_float(b);
+}
+__device__ __forceinline__ uint64_t mul2u(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2u(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
 
@@ -299,6 +319,8 @@ struct Params {
 struct Item {
     int p, r0, rows, ncols, w0;  // slot, first row, valid rows, MMA N, first weight row
 };
+
+
 
 template <bool GU>
 __device__ __forceinline__ Item load_item(const Params& P, int it) {
@@ -367,12 +389,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---- producer duty (thread 0): issue every raw stage whose slot is free.
     // Never blocks; called at each step and from inside thread 0's waits.
     int next_stage = 0;
+    int4* ring = (int4*)(smem + L::O_ITEMS);
+    // item i as (slot, first row, valid rows, first weight row); written by thread 0
+    // before the first TMA of the item, read by everyone after a barrier that
+    // orders them after that TMA
+    auto item = [&](int i) -> Item {
+        const int4 v = ring[i % ITEM_RING];
+        Item I;
+        I.p = v.x;
+        I.r0 = v.y;
+        I.rows = v.z;
+        I.ncols = (v.z + 15) & ~15;
+        I.w0 = v.w;
+        return I;
+    };
     auto produce = [&]() {
         while (next_stage < total_stages) {
             const int gs = next_stage, sl = gs % RS, u = gs / RS;
             if (u > 0 && !mbar_try_wait(bar(B_RAW_EMPTY + sl), (u - 1) & 1)) return;
             const int i = gs / spi, s = gs - i * spi;
-            const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
+            if (s == 0) {
+                const Item J = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
+                ring[i % ITEM_RING] = make_int4(J.p, J.r0, J.rows, J.w0);
+            }
+            const Item I = item(i);
             const uint32_t st = sbase + sl * L::STAGE;
             const uint32_t fb = bar(B_RAW_FULL + sl);
             mbar_expect_tx(fb, L::TX);
@@ -390,13 +430,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             ++next_stage;
         }
     };
-    // bounded wait; thread 0 keeps producing while it waits
+    // bounded wait; thread 0 keeps producing while it waits, the others sleep
     auto waitp = [&](uint32_t b, uint32_t parity) -> bool {
         if (mbar_try_wait(b, parity)) return true;
         long long t0 = clock64();
         while (true) {
-            if (is_producer) produce();
-            if (mbar_try_wait(b, parity)) return true;
+            if (is_producer) {
+                produce();
+                if (mbar_try_wait(b, parity)) return true;
+            } else if (mbar_try_wait_sleep(b, parity)) {
+                return true;
+            }
             if (*abort_flag) return false;
             if (clock64() - t0 > TIMEOUT_CYCLES) {
                 *abort_flag = 1;
@@ -408,11 +452,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---- MMA duty (thread 32): block idx's products into TMEM buffer idx % 2.
     int mma_issued = 0;
     auto issue_mma = [&](int idx) -> bool {
-        const Item I = load_item<GU>(P, (int)blockIdx.x + (idx / nb) * (int)gridDim.x);
         const int sl = idx % NF, u = idx / NF;
         if (!waitp(bar(B_F16_FULL + sl), u & 1)) return false;
         if (u > 0 && !waitp(bar(B_TM_EMPTY + sl), (u - 1) & 1)) return false;
         tc_fence_after();
+        const Item I = item(idx / nb);  // read after the barrier that orders it
         const uint32_t fa = sbase + L::O_F16 + sl * F16_SLOT;
         const uint32_t fbB = fa + F16_A;
         const uint32_t id = idesc_f16(BM, I.ncols);
@@ -434,17 +478,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int h = warp >> 2;        // column half
     const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
-    float accA[4][16], accB[4][16];
+    // accumulators: 4 chunks x 16 columns for each matrix, as 8 packed pairs
+    uint64_t accA[4][8], accB[4][8];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) accA[c][j] = accB[c][j] = 0.0f;
+        for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
 
     auto convert = [&](int idx) -> bool {
-        const int i = idx / nb;
-        const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
         const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
         if (!waitp(bar(B_RAW_FULL + sl), (gs / RS) & 1)) return false;
+        const Item I = item(idx / nb);  // read after the barrier that orders it
         const uint8_t* st = smem + sl * L::STAGE;
         uint8_t* fa = smem + L::O_F16 + (idx % NF) * F16_SLOT;
         uint8_t* fbB = fa + F16_A;
@@ -520,28 +564,34 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     auto epilogue = [&](int idx) -> bool {
         const int i = idx / nb, b = idx - i * nb;
-        const Item I = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
         const int sl = idx % NF;
         // warp-uniform decision: the TMEM loads below are warp-collective
         if (!__all_sync(0xffffffffu, waitp(bar(B_TM_FULL + sl), (idx / NF) & 1))) return false;
         tc_fence_after();
+        const Item I = item(i);
         const float* sc = (const float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
         const float dA = sc[m], dB = sc[BM + m];
         const float mA = WT == MOE_W_Q4_1 ? sc[2 * BM + m] : 0.0f;
         const float mB = WT == MOE_W_Q4_1 ? sc[3 * BM + m] : 0.0f;
-        const float* dX = sc + 4 * BM;
-        const float* sX = sc + 4 * BM + BN;
+        const uint64_t dA2 = pk2(__float_as_uint(dA), __float_as_uint(dA));
+        const uint64_t dB2 = pk2(__float_as_uint(dB), __float_as_uint(dB));
+        const uint64_t mA2 = pk2(__float_as_uint(mA), __float_as_uint(mA));
+        const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
+        const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
+        const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + sl * 256;
         const int nch = min(4, max(0, (I.ncols - h * 64) / 16));  // active 16-column chunks
-        // software pipeline: chunk c+1's TMEM loads are in flight while chunk c is scaled
+        // software pipeline: chunk c+1's TMEM loads (and scales) are in flight
+        // while chunk c is scaled and accumulated
         uint32_t ra[2][16], rb[2][16];
+        uint64_t dxp[8];
         if (nch > 0) {
             tmem_ld16(tbase + h * 64, ra[0]);
             tmem_ld16(tbase + 128 + h * 64, rb[0]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dxp[j] = dX2[h * 32 + j];
             tmem_wait32(ra[0], rb[0]);
         }
-        const float2 dA2 = make_float2(dA, dA), dB2 = make_float2(dB, dB);
-        const float2 mA2 = make_float2(mA, mA), mB2 = make_float2(mB, mB);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             if (c < nch) {
@@ -551,37 +601,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld16(tbase + col0 + 16, ra[nxt]);
                     tmem_ld16(tbase + 128 + col0 + 16, rb[nxt]);
                 }
-                const float4* dx4 = reinterpret_cast<const float4*>(dX + col0);
-                const float4* sx4 = reinterpret_cast<const float4*>(sX + col0);
 #pragma unroll
-                for (int j4 = 0; j4 < 4; ++j4) {
-                    const float4 dx = dx4[j4];
-                    const float2 dlo = make_float2(dx.x, dx.y), dhi = make_float2(dx.z, dx.w);
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = j4 * 4 + e * 2;
-                        const float2 d2 = e ? dhi : dlo;
-                        const float2 pa = make_float2(__uint_as_float(ra[cur][j]),
-                                                      __uint_as_float(ra[cur][j + 1]));
-                        const float2 pb = make_float2(__uint_as_float(rb[cur][j]),
-                                                      __uint_as_float(rb[cur][j + 1]));
-                        float2 xa = make_float2(accA[c][j], accA[c][j + 1]);
-                        float2 xb = make_float2(accB[c][j], accB[c][j + 1]);
-                        xa = fma2(mul2(dA2, d2), pa, xa);
-                        xb = fma2(mul2(dB2, d2), pb, xb);
-                        if (WT == MOE_W_Q4_1) {
-                            const float4 sx = sx4[j4];
-                            const float2 s2 = e ? make_float2(sx.z, sx.w) : make_float2(sx.x, sx.y);
-                            xa = fma2(mA2, s2, xa);
-                            xb = fma2(mB2, s2, xb);
-                        }
-                        accA[c][j] = xa.x;
-                        accA[c][j + 1] = xa.y;
-                        accB[c][j] = xb.x;
-                        accB[c][j + 1] = xb.y;
+                for (int j = 0; j < 8; ++j) {
+                    const uint64_t pa = pk2(ra[cur][2 * j], ra[cur][2 * j + 1]);
+                    const uint64_t pb = pk2(rb[cur][2 * j], rb[cur][2 * j + 1]);
+                    accA[c][j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[c][j]);
+                    accB[c][j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[c][j]);
+                    if (WT == MOE_W_Q4_1) {
+                        const uint64_t s2 = sX2[col0 / 2 + j];
+                        accA[c][j] = fma2u(mA2, s2, accA[c][j]);
+                        accB[c][j] = fma2u(mB2, s2, accB[c][j]);
                     }
                 }
-                if (c + 1 < nch) tmem_wait32(ra[nxt], rb[nxt]);
+                if (c + 1 < nch) {
+                    // next chunk's scales load while its TMEM loads complete
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) dxp[j] = dX2[(col0 + 16) / 2 + j];
+                    tmem_wait32(ra[nxt], rb[nxt]);
+                }
             }
         }
         tc_fence_before();
@@ -591,18 +628,24 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int n = h * 64 + c * 16 + j;
-                    if (n < I.rows) {
-                        float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
-                        if (GU) {
-                            o[0] = silu_mul(accA[c][j], accB[c][j]);
-                        } else {
-                            o[0] = accA[c][j];
-                            o[BM] = accB[c][j];
+                for (int j = 0; j < 8; ++j) {
+                    float a[2], bb[2];
+                    upk2(accA[c][j], a[0], a[1]);
+                    upk2(accB[c][j], bb[0], bb[1]);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int n = h * 64 + c * 16 + 2 * j + e;
+                        if (n < I.rows) {
+                            float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
+                            if (GU) {
+                                o[0] = silu_mul(a[e], bb[e]);
+                            } else {
+                                o[0] = a[e];
+                                o[BM] = bb[e];
+                            }
                         }
                     }
-                    accA[c][j] = accB[c][j] = 0.0f;
+                    accA[c][j] = accB[c][j] = 0ull;
                 }
             }
         }
