@@ -13,19 +13,19 @@
 // integer.  The per-block fp32 scaling then runs on the CUDA cores in the same
 // order as the scalar definition: acc = fma(dW*dx, I_b, acc) (+ fma(mW, sx, acc)).
 //
-// One persistent CTA of 8 warps per SM (static round-robin over the
+// One persistent CTA of 16 warps per SM (static round-robin over the
 // device-built, longest-first work list).  A work item is 128 tokens of one
 // expert times two 128-row weight blocks (gate and up rows j0..j0+127 for
 // stage 4; down rows i0..i0+255 for stage 6).  Every warp is a worker: for
 // 32-block b it reads its quarter of the TMEM lanes (its weight rows) for its
-// half of the columns (tokens), scales and accumulates in registers (128 fp32
-// per thread), then converts block b+2's raw tiles into the fp16 operand
-// layout.  Two threads carry extra duties: thread 0 issues the TMA loads of
+// group of 32 columns (tokens), scales and accumulates in registers (64 fp32
+// per thread), then converts its share of block b+2's raw tiles into the fp16
+// operand layout.  Two threads carry extra duties: thread 0 issues the TMA loads of
 // raw int8 / 4-bit tiles and fp16 scales (4 blocks a stage, never blocking),
 // thread 32 issues block b+1's MMAs -- 2 x (M=128, N<=128, K=16) per matrix --
 // into the TMEM buffer the workers are not reading, committed to an mbarrier.
-// (The register file is split over the four SM sub-partitions, so 8 warps of
-// up to 255 registers fit where 10 warps of 200 would not.)
+// (The register file is split over the four SM sub-partitions: 16 warps of up
+// to 128 registers fill it, four warps per sub-partition to hide latency.)
 // Every wait is bounded: on timeout the kernel sets MOE_DEV_ERR_TIMEOUT, drains
 // what it started and exits.
 #include <cudaTypedefs.h>
@@ -45,7 +45,7 @@ constexpr int KBS = 4;       // 32-blocks per raw stage
 constexpr int RS = 3;        // raw stages
 constexpr int NF = 2;        // fp16 operand slots = TMEM partial buffers
 constexpr int NSC = 4;       // scale ring slots
-constexpr int THREADS = 256; // 8 warps, 2 per SM sub-partition
+constexpr int THREADS = 512; // 16 warps, 4 per SM sub-partition, <= 128 registers each
 constexpr int LOOKAHEAD = 2; // blocks converted ahead of the epilogue
 constexpr int ITEM_RING = 8; // work items kept in shared memory (written by the producer)
 constexpr long long TIMEOUT_CYCLES = 1LL << 32;
@@ -474,14 +474,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
 
     // ---- worker duty (all threads)
-    const int wt = threadIdx.x;     // 0..255
+    const int wt = threadIdx.x;     // 0..511
     const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int h = warp >> 2;        // column half
+    const int g = warp >> 2;        // column group: tokens 32g .. 32g+31
     const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
-    // accumulators: 4 chunks x 16 columns for each matrix, as 8 packed pairs
-    uint64_t accA[4][8], accB[4][8];
+    // accumulators: 2 chunks x 16 columns for each matrix, as 8 packed pairs
+    uint64_t accA[2][8], accB[2][8];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
 
@@ -495,23 +495,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         float* sc = (float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
         // weights: 256 rows x 32 values of block blk
         if (WT == MOE_W_Q8_0) {
-#pragma unroll
-            for (int rep = 0; rep < 2; ++rep) {
-                const int u = wt + rep * 256;
-                const int R = u >> 1, hh = u & 1;
-                const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
-                const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
-                uint4 o0, o1;
-                cvt_i8x4(v.x, o0.x, o0.y);
-                cvt_i8x4(v.y, o0.z, o0.w);
-                cvt_i8x4(v.z, o1.x, o1.y);
-                cvt_i8x4(v.w, o1.z, o1.w);
-                uint8_t* dst = fa + (R >> 7) * (BM * 64);
-                *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
-                *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
-            }
-        } else {
-            const int R = wt;
+            const int R = wt >> 1, hh = wt & 1;       // 512 units of 16 values
+            const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
+            const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
+            uint4 o0, o1;
+            cvt_i8x4(v.x, o0.x, o0.y);
+            cvt_i8x4(v.y, o0.z, o0.w);
+            cvt_i8x4(v.z, o1.x, o1.y);
+            cvt_i8x4(v.w, o1.z, o1.w);
+            uint8_t* dst = fa + (R >> 7) * (BM * 64);
+            *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
+            *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
+        } else if (wt < 2 * BM) {
+            const int R = wt;                     // 256 units of 32 values
             const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
             const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -545,7 +541,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             *(uint4*)(fbB + f16_off(n, 2 * hh + 1)) = o1;
         }
         // scales of block blk as fp32: dW[256], mW[256], dX[128], sX[128]
-        {
+        if (wt < 2 * BM) {
             const int R = wt;
             const int si = GU ? (((R >> 7) * KBS + blk) * BM + (R & 127)) : (blk * 2 * BM + R);
             sc[R] = __half2float(((const __half*)(st + L::O_WS))[si]);
@@ -580,31 +576,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
         const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + sl * 256;
-        const int nch = min(4, max(0, (I.ncols - h * 64) / 16));  // active 16-column chunks
-        // software pipeline: chunk c+1's TMEM loads (and scales) are in flight
-        // while chunk c is scaled and accumulated
-        uint32_t ra[2][16], rb[2][16];
-        uint64_t dxp[8];
-        if (nch > 0) {
-            tmem_ld16(tbase + h * 64, ra[0]);
-            tmem_ld16(tbase + 128 + h * 64, rb[0]);
+        const int nch = min(2, max(0, (I.ncols - g * 32) / 16));  // active 16-column chunks
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dxp[j] = dX2[h * 32 + j];
-            tmem_wait32(ra[0], rb[0]);
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
             if (c < nch) {
-                const int cur = c & 1, nxt = cur ^ 1;
-                const int col0 = h * 64 + c * 16;
-                if (c + 1 < nch) {
-                    tmem_ld16(tbase + col0 + 16, ra[nxt]);
-                    tmem_ld16(tbase + 128 + col0 + 16, rb[nxt]);
-                }
+                const int col0 = g * 32 + c * 16;
+                uint32_t ra[16], rb[16];
+                tmem_ld16(tbase + col0, ra);
+                tmem_ld16(tbase + 128 + col0, rb);
+                uint64_t dxp[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dxp[j] = dX2[col0 / 2 + j];
+                tmem_wait32(ra, rb);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const uint64_t pa = pk2(ra[cur][2 * j], ra[cur][2 * j + 1]);
-                    const uint64_t pb = pk2(rb[cur][2 * j], rb[cur][2 * j + 1]);
+                    const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
+                    const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
                     accA[c][j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[c][j]);
                     accB[c][j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[c][j]);
                     if (WT == MOE_W_Q4_1) {
@@ -613,12 +600,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                         accB[c][j] = fma2u(mB2, s2, accB[c][j]);
                     }
                 }
-                if (c + 1 < nch) {
-                    // next chunk's scales load while its TMEM loads complete
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) dxp[j] = dX2[(col0 + 16) / 2 + j];
-                    tmem_wait32(ra[nxt], rb[nxt]);
-                }
             }
         }
         tc_fence_before();
@@ -626,7 +607,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (b == nb - 1) {
             // item complete: write this thread's row for every valid token
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     float a[2], bb[2];
@@ -634,7 +615,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     upk2(accB[c][j], bb[0], bb[1]);
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int n = h * 64 + c * 16 + 2 * j + e;
+                        const int n = g * 32 + c * 16 + 2 * j + e;
                         if (n < I.rows) {
                             float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
                             if (GU) {
