@@ -39,21 +39,23 @@
 namespace moe {
 namespace tc {
 
-constexpr int BN = 128;      // tokens per work item (TMEM columns per matrix)
+constexpr int BN = 64;       // tokens per work item (TMEM columns per matrix)
 constexpr int BM = 128;      // weight rows per matrix (TMEM lanes)
 constexpr int KBS = 4;       // 32-blocks per raw stage
-constexpr int RS = 3;        // raw stages
-constexpr int NF = 2;        // fp16 operand slots = TMEM partial buffers
-constexpr int NSC = 4;       // scale ring slots
+constexpr int RS = 2;        // raw stages
+constexpr int NB = 4;        // TMEM partial buffers (2 matrices x BN columns each)
+constexpr int NF = 4;        // fp16 operand slots = blocks converted ahead of the epilogue
+constexpr int NSC = 2 * NF;  // scale ring slots (a slot is reused 2*NF blocks later)
 constexpr int THREADS = 512; // 16 warps, 4 per SM sub-partition, <= 128 registers each
-constexpr int LOOKAHEAD = 2; // blocks converted ahead of the epilogue
+constexpr int NWARPS = THREADS / 32;  // consumer barriers count one arrival per warp
+constexpr int LOOKAHEAD = NF;
 constexpr int ITEM_RING = 8; // work items kept in shared memory (written by the producer)
 constexpr long long TIMEOUT_CYCLES = 1LL << 32;
 
 constexpr int F16_A = 2 * BM * 64;  // two 128-row matrices x 32 fp16
 constexpr int F16_B = BN * 64;
 constexpr int F16_SLOT = F16_A + F16_B;
-constexpr int SC_SLOT = (2 * BM * 2 + BN * 2) * 4;  // dW, mW [256]; dX, sX [128] (fp32)
+constexpr int SC_SLOT = (2 * BM * 2 + BN * 2) * 4;  // dW, mW [256]; dX, sX [BN] (fp32)
 
 __host__ __device__ constexpr int cround(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -75,7 +77,7 @@ struct Lay {
     static constexpr int O_F16 = RS * STAGE;
     static constexpr int O_SC = O_F16 + NF * F16_SLOT;
     static constexpr int O_BAR = O_SC + NSC * SC_SLOT;
-    static constexpr int N_BARS = 2 * RS + 3 * NF;
+    static constexpr int N_BARS = 2 * RS + NF + 2 * NB;
     static constexpr int O_ITEMS = cround(O_BAR + N_BARS * 8 + 16, 16);
     static constexpr int SMEM = O_ITEMS + ITEM_RING * 16 + 1024;  // + alignment slack
 };
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int B_RAW_FULL = 0, B_RAW_EMPTY = RS, B_F16_FULL = 2 * RS, B_TM_FULL = 2 * RS + NF,
-              B_TM_EMPTY = 2 * RS + 2 * NF;
+              B_TM_EMPTY = 2 * RS + NF + NB;
 
     const int n_items = *P.n_tiles * P.mt_count;
     if ((int)blockIdx.x >= n_items) return;
@@ -365,12 +367,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
             mbar_init(bar(B_RAW_FULL + i), 1);
-            mbar_init(bar(B_RAW_EMPTY + i), THREADS);
+            mbar_init(bar(B_RAW_EMPTY + i), NWARPS);
         }
-        for (int i = 0; i < NF; ++i) {
-            mbar_init(bar(B_F16_FULL + i), THREADS);
+        for (int i = 0; i < NF; ++i) mbar_init(bar(B_F16_FULL + i), NWARPS);
+        for (int i = 0; i < NB; ++i) {
             mbar_init(bar(B_TM_FULL + i), 1);
-            mbar_init(bar(B_TM_EMPTY + i), THREADS);
+            mbar_init(bar(B_TM_EMPTY + i), NWARPS);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -430,13 +432,42 @@ __global__ void __launch_bounds__(THREADS, 1)
             ++next_stage;
         }
     };
-    // bounded wait; thread 0 keeps producing while it waits, the others sleep
+    // ---- MMA duty (thread 32): issue, in order, every block whose fp16 operands
+    // are complete and whose TMEM buffer (idx % NB) has been drained; never blocks.
+    int next_mma = 0;
+    auto mma_try = [&]() {
+        while (next_mma < total) {
+            const int idx = next_mma;
+            const int fs = idx % NF, tb = idx % NB;
+            if (!mbar_try_wait(bar(B_F16_FULL + fs), (idx / NF) & 1)) return;
+            if (idx >= NB && !mbar_try_wait(bar(B_TM_EMPTY + tb), ((idx / NB) - 1) & 1)) return;
+            tc_fence_after();
+            const Item I = item(idx / nb);  // ordered by the f16_full barrier
+            const uint32_t fa = sbase + L::O_F16 + fs * F16_SLOT;
+            const uint32_t fbB = fa + F16_A;
+            const uint32_t id = idesc_f16(BM, I.ncols);
+#pragma unroll
+            for (int mat = 0; mat < 2; ++mat) {
+#pragma unroll
+                for (int k16 = 0; k16 < 2; ++k16) {
+                    mma_f16(tmem + tb * (2 * BN) + mat * BN,
+                            sdesc(fa + mat * (BM * 64) + k16 * 256, 128, 512),
+                            sdesc(fbB + k16 * 256, 128, 512), id, (uint32_t)k16);
+                }
+            }
+            mma_commit(bar(B_TM_FULL + tb));
+            ++next_mma;
+        }
+    };
+    // bounded wait; threads 0 and 32 keep producing / issuing while they wait,
+    // the others sleep in hardware
     auto waitp = [&](uint32_t b, uint32_t parity) -> bool {
         if (mbar_try_wait(b, parity)) return true;
         long long t0 = clock64();
         while (true) {
-            if (is_producer) {
-                produce();
+            if (is_producer || is_mma) {
+                if (is_producer) produce();
+                else mma_try();
                 if (mbar_try_wait(b, parity)) return true;
             } else if (mbar_try_wait_sleep(b, parity)) {
                 return true;
@@ -449,45 +480,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     };
 
-    // ---- MMA duty (thread 32): block idx's products into TMEM buffer idx % 2.
-    int mma_issued = 0;
-    auto issue_mma = [&](int idx) -> bool {
-        const int sl = idx % NF, u = idx / NF;
-        if (!waitp(bar(B_F16_FULL + sl), u & 1)) return false;
-        if (u > 0 && !waitp(bar(B_TM_EMPTY + sl), (u - 1) & 1)) return false;
-        tc_fence_after();
-        const Item I = item(idx / nb);  // read after the barrier that orders it
-        const uint32_t fa = sbase + L::O_F16 + sl * F16_SLOT;
-        const uint32_t fbB = fa + F16_A;
-        const uint32_t id = idesc_f16(BM, I.ncols);
-#pragma unroll
-        for (int mat = 0; mat < 2; ++mat) {
-#pragma unroll
-            for (int k16 = 0; k16 < 2; ++k16) {
-                mma_f16(tmem + sl * 256 + mat * 128, sdesc(fa + mat * (BM * 64) + k16 * 256, 128, 512),
-                        sdesc(fbB + k16 * 256, 128, 512), id, (uint32_t)k16);
-            }
-        }
-        mma_commit(bar(B_TM_FULL + sl));
-        mma_issued = idx + 1;
-        return true;
-    };
-
     // ---- worker duty (all threads)
     const int wt = threadIdx.x;     // 0..511
     const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int g = warp >> 2;        // column group: tokens 32g .. 32g+31
+    const int g = warp >> 2;        // column group: tokens 16g .. 16g+15
     const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
-    // accumulators: 2 chunks x 16 columns for each matrix, as 8 packed pairs
-    uint64_t accA[2][8], accB[2][8];
+    // accumulators: 16 columns for each matrix, as 8 packed pairs
+    uint64_t accA[8], accB[8];
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
+    for (int j = 0; j < 8; ++j) accA[j] = accB[j] = 0ull;
 
     auto convert = [&](int idx) -> bool {
         const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
-        if (!waitp(bar(B_RAW_FULL + sl), (gs / RS) & 1)) return false;
+        // warp-uniform decision: the warp synchronizes below before arriving
+        if (!__all_sync(0xffffffffu, waitp(bar(B_RAW_FULL + sl), (gs / RS) & 1))) return false;
         const Item I = item(idx / nb);  // read after the barrier that orders it
         const uint8_t* st = smem + sl * L::STAGE;
         uint8_t* fa = smem + L::O_F16 + (idx % NF) * F16_SLOT;
@@ -552,17 +558,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                 sc[4 * BM + BN + R] = __high2float(xs);
             }
         }
+        // make this thread's fp16 operands visible to the tensor core, then one
+        // arrival per warp (an mbarrier is a single word: 512 arrivals serialize)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(bar(B_F16_FULL + idx % NF));
-        if (blk == KBS - 1) mbar_arrive(bar(B_RAW_EMPTY + sl));
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(bar(B_F16_FULL + idx % NF));
+            if (blk == KBS - 1) mbar_arrive(bar(B_RAW_EMPTY + sl));
+        }
         return true;
     };
 
     auto epilogue = [&](int idx) -> bool {
         const int i = idx / nb, b = idx - i * nb;
-        const int sl = idx % NF;
+        const int tb = idx % NB;
         // warp-uniform decision: the TMEM loads below are warp-collective
-        if (!__all_sync(0xffffffffu, waitp(bar(B_TM_FULL + sl), (idx / NF) & 1))) return false;
+        if (!__all_sync(0xffffffffu, waitp(bar(B_TM_FULL + tb), (idx / NB) & 1))) return false;
         tc_fence_after();
         const Item I = item(i);
         const float* sc = (const float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
@@ -575,59 +586,53 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
         const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
         const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
-        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + sl * 256;
-        const int nch = min(2, max(0, (I.ncols - g * 32) / 16));  // active 16-column chunks
+        const int col0 = g * 16;
+        if (col0 < I.ncols) {
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + tb * (2 * BN) + col0;
+            uint32_t ra[16], rb[16];
+            tmem_ld16(taddr, ra);
+            tmem_ld16(taddr + BN, rb);
+            uint64_t dxp[8];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            if (c < nch) {
-                const int col0 = g * 32 + c * 16;
-                uint32_t ra[16], rb[16];
-                tmem_ld16(tbase + col0, ra);
-                tmem_ld16(tbase + 128 + col0, rb);
-                uint64_t dxp[8];
+            for (int j = 0; j < 8; ++j) dxp[j] = dX2[col0 / 2 + j];
+            tmem_wait32(ra, rb);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) dxp[j] = dX2[col0 / 2 + j];
-                tmem_wait32(ra, rb);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
-                    const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
-                    accA[c][j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[c][j]);
-                    accB[c][j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[c][j]);
-                    if (WT == MOE_W_Q4_1) {
-                        const uint64_t s2 = sX2[col0 / 2 + j];
-                        accA[c][j] = fma2u(mA2, s2, accA[c][j]);
-                        accB[c][j] = fma2u(mB2, s2, accB[c][j]);
-                    }
+            for (int j = 0; j < 8; ++j) {
+                const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
+                const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
+                accA[j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[j]);
+                accB[j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[j]);
+                if (WT == MOE_W_Q4_1) {
+                    const uint64_t s2 = sX2[col0 / 2 + j];
+                    accA[j] = fma2u(mA2, s2, accA[j]);
+                    accB[j] = fma2u(mB2, s2, accB[j]);
                 }
             }
         }
         tc_fence_before();
-        mbar_arrive(bar(B_TM_EMPTY + sl));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_TM_EMPTY + tb));
         if (b == nb - 1) {
             // item complete: write this thread's row for every valid token
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int j = 0; j < 8; ++j) {
+                float a[2], bb[2];
+                upk2(accA[j], a[0], a[1]);
+                upk2(accB[j], bb[0], bb[1]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float a[2], bb[2];
-                    upk2(accA[c][j], a[0], a[1]);
-                    upk2(accB[c][j], bb[0], bb[1]);
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int n = g * 32 + c * 16 + 2 * j + e;
-                        if (n < I.rows) {
-                            float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
-                            if (GU) {
-                                o[0] = silu_mul(a[e], bb[e]);
-                            } else {
-                                o[0] = a[e];
-                                o[BM] = bb[e];
-                            }
+                for (int e = 0; e < 2; ++e) {
+                    const int n = col0 + 2 * j + e;
+                    if (n < I.rows) {
+                        float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
+                        if (GU) {
+                            o[0] = silu_mul(a[e], bb[e]);
+                        } else {
+                            o[0] = a[e];
+                            o[BM] = bb[e];
                         }
                     }
-                    accA[c][j] = accB[c][j] = 0ull;
                 }
+                accA[j] = accB[j] = 0ull;
             }
         }
         return true;
@@ -639,14 +644,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     // next waits observe.
     bool ok = true;
     if (is_producer) produce();
-    for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx)
-        ok = __all_sync(0xffffffffu, convert(idx));
-    if (ok && is_mma) issue_mma(0);
+    for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx) ok = convert(idx);
     for (int idx = 0; idx < total && ok; ++idx) {
         if (is_producer) produce();
-        if (is_mma && idx + 1 < total) issue_mma(idx + 1);
+        if (is_mma) mma_try();
         ok = epilogue(idx);
-        if (ok && idx + LOOKAHEAD < total) ok = __all_sync(0xffffffffu, convert(idx + LOOKAHEAD));
+        if (ok && idx + LOOKAHEAD < total) ok = convert(idx + LOOKAHEAD);
+    }
+    // every MMA must be issued before the CTA drains (thread 32 finishes the tail)
+    if (is_mma) {
+        long long t0 = clock64();
+        while (next_mma < total && !*abort_flag && clock64() - t0 < TIMEOUT_CYCLES) mma_try();
     }
 
     // drain what this CTA started before it may exit (only waits on the abort path)
@@ -658,10 +666,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     }
-    if (is_mma && mma_issued > 0) {
-        const int last = mma_issued - 1;
+    if (is_mma && next_mma > 0) {  // the last commit covers every MMA issued before it
+        const int last = next_mma - 1;
         long long t0 = clock64();
-        while (!mbar_try_wait(bar(B_TM_FULL + last % NF), (last / NF) & 1) &&
+        while (!mbar_try_wait(bar(B_TM_FULL + last % NB), (last / NB) & 1) &&
                clock64() - t0 < TIMEOUT_CYCLES) {
         }
     }
