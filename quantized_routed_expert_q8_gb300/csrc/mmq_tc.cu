@@ -116,6 +116,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of a phase (mbarrier.try_wait may suspend the thread for a
+// system-dependent time; test_wait never does).  Used by the threads that poll
+// several barriers in turn: the TMA producer and the MMA issuer.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // As mbar_try_wait, but the thread may sleep in hardware (up to ~20 us) until
 // the phase completes instead of spinning on the issue slots.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
@@ -408,7 +422,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto produce = [&]() {
         while (next_stage < total_stages) {
             const int gs = next_stage, sl = gs % RS, u = gs / RS;
-            if (u > 0 && !mbar_try_wait(bar(B_RAW_EMPTY + sl), (u - 1) & 1)) return;
+            if (u > 0 && !mbar_test_wait(bar(B_RAW_EMPTY + sl), (u - 1) & 1)) return;
             const int i = gs / spi, s = gs - i * spi;
             if (s == 0) {
                 const Item J = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
@@ -439,8 +453,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         while (next_mma < total) {
             const int idx = next_mma;
             const int fs = idx % NF, tb = idx % NB;
-            if (!mbar_try_wait(bar(B_F16_FULL + fs), (idx / NF) & 1)) return;
-            if (idx >= NB && !mbar_try_wait(bar(B_TM_EMPTY + tb), ((idx / NB) - 1) & 1)) return;
+            if (!mbar_test_wait(bar(B_F16_FULL + fs), (idx / NF) & 1)) return;
+            if (idx >= NB && !mbar_test_wait(bar(B_TM_EMPTY + tb), ((idx / NB) - 1) & 1)) return;
             tc_fence_after();
             const Item I = item(idx / nb);  // ordered by the f16_full barrier
             const uint32_t fa = sbase + L::O_F16 + fs * F16_SLOT;
@@ -462,13 +476,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     // bounded wait; threads 0 and 32 keep producing / issuing while they wait,
     // the others sleep in hardware
     auto waitp = [&](uint32_t b, uint32_t parity) -> bool {
-        if (mbar_try_wait(b, parity)) return true;
+        if (mbar_test_wait(b, parity)) return true;
         long long t0 = clock64();
         while (true) {
             if (is_producer || is_mma) {
                 if (is_producer) produce();
                 else mma_try();
-                if (mbar_try_wait(b, parity)) return true;
+                if (mbar_test_wait(b, parity)) return true;
             } else if (mbar_try_wait_sleep(b, parity)) {
                 return true;
             }
