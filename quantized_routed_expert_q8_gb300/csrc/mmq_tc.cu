@@ -46,8 +46,9 @@ constexpr int RS = 2;        // raw stages
 constexpr int NB = 4;        // TMEM partial buffers (2 matrices x BN columns each)
 constexpr int NF = 4;        // fp16 operand slots = blocks converted ahead of the epilogue
 constexpr int NSC = 2 * NF;  // scale ring slots (a slot is reused 2*NF blocks later)
-constexpr int THREADS = 512; // 16 warps, 4 per SM sub-partition, <= 128 registers each
-constexpr int NWARPS = THREADS / 32;  // consumer barriers count one arrival per warp
+constexpr int NWORK = 8;                      // worker warps (convert + epilogue)
+constexpr int THREADS = 32 * (NWORK + 1);     // + one control warp (TMA and MMA issue)
+constexpr int NWARPS = NWORK;                 // consumer barriers count one arrival per worker warp
 constexpr int LOOKAHEAD = NF;
 constexpr int ITEM_RING = 8; // work items kept in shared memory (written by the producer)
 constexpr long long TIMEOUT_CYCLES = 1LL << 32;
@@ -375,8 +376,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int total = my_items * nb;
     const int total_stages = my_items * spi;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool is_producer = threadIdx.x == 0;
-    const bool is_mma = threadIdx.x == 32;
+    const bool is_control = warp == NWORK;  // the last warp issues TMA loads and MMAs
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
@@ -473,19 +473,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             ++next_mma;
         }
     };
-    // bounded wait; threads 0 and 32 keep producing / issuing while they wait,
-    // the others sleep in hardware
+    // bounded wait of a worker thread (sleeps in hardware between probes)
     auto waitp = [&](uint32_t b, uint32_t parity) -> bool {
         if (mbar_test_wait(b, parity)) return true;
         long long t0 = clock64();
         while (true) {
-            if (is_producer || is_mma) {
-                if (is_producer) produce();
-                else mma_try();
-                if (mbar_test_wait(b, parity)) return true;
-            } else if (mbar_try_wait_sleep(b, parity)) {
-                return true;
-            }
+            if (mbar_try_wait_sleep(b, parity)) return true;
             if (*abort_flag) return false;
             if (clock64() - t0 > TIMEOUT_CYCLES) {
                 *abort_flag = 1;
@@ -494,15 +487,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     };
 
-    // ---- worker duty (all threads)
-    const int wt = threadIdx.x;     // 0..511
+    // ---- worker duty (warps 0 .. NWORK-1)
+    const int wt = threadIdx.x;     // 0..255 for workers
     const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int g = warp >> 2;        // column group: tokens 16g .. 16g+15
+    const int h = (warp >> 2) & 1;  // column half: tokens 32h .. 32h+31
     const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
-    // accumulators: 16 columns for each matrix, as 8 packed pairs
-    uint64_t accA[8], accB[8];
+    // accumulators: 2 chunks x 16 columns for each matrix, as 8 packed pairs
+    uint64_t accA[2][8], accB[2][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) accA[j] = accB[j] = 0ull;
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
 
     auto convert = [&](int idx) -> bool {
         const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
@@ -515,18 +510,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         float* sc = (float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
         // weights: 256 rows x 32 values of block blk
         if (WT == MOE_W_Q8_0) {
-            const int R = wt >> 1, hh = wt & 1;       // 512 units of 16 values
-            const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
-            const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
-            uint4 o0, o1;
-            cvt_i8x4(v.x, o0.x, o0.y);
-            cvt_i8x4(v.y, o0.z, o0.w);
-            cvt_i8x4(v.z, o1.x, o1.y);
-            cvt_i8x4(v.w, o1.z, o1.w);
-            uint8_t* dst = fa + (R >> 7) * (BM * 64);
-            *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
-            *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
-        } else if (wt < 2 * BM) {
+#pragma unroll
+            for (int rep = 0; rep < 2; ++rep) {
+                const int u = wt + rep * 256;             // 512 units of 16 values
+                const int R = u >> 1, hh = u & 1;
+                const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
+                const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
+                uint4 o0, o1;
+                cvt_i8x4(v.x, o0.x, o0.y);
+                cvt_i8x4(v.y, o0.z, o0.w);
+                cvt_i8x4(v.z, o1.x, o1.y);
+                cvt_i8x4(v.w, o1.z, o1.w);
+                uint8_t* dst = fa + (R >> 7) * (BM * 64);
+                *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
+                *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
+            }
+        } else {
             const int R = wt;                     // 256 units of 32 values
             const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
             const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
@@ -600,26 +599,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
         const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
         const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
-        const int col0 = g * 16;
-        if (col0 < I.ncols) {
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + tb * (2 * BN) + col0;
-            uint32_t ra[16], rb[16];
-            tmem_ld16(taddr, ra);
-            tmem_ld16(taddr + BN, rb);
-            uint64_t dxp[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dxp[j] = dX2[col0 / 2 + j];
-            tmem_wait32(ra, rb);
+        for (int c = 0; c < 2; ++c) {
+            const int col0 = h * 32 + c * 16;
+            if (col0 < I.ncols) {
+                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + tb * (2 * BN) + col0;
+                uint32_t ra[16], rb[16];
+                tmem_ld16(taddr, ra);
+                tmem_ld16(taddr + BN, rb);
+                uint64_t dxp[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
-                const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
-                accA[j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[j]);
-                accB[j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[j]);
-                if (WT == MOE_W_Q4_1) {
-                    const uint64_t s2 = sX2[col0 / 2 + j];
-                    accA[j] = fma2u(mA2, s2, accA[j]);
-                    accB[j] = fma2u(mB2, s2, accB[j]);
+                for (int j = 0; j < 8; ++j) dxp[j] = dX2[col0 / 2 + j];
+                tmem_wait32(ra, rb);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
+                    const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
+                    accA[c][j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[c][j]);
+                    accB[c][j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[c][j]);
+                    if (WT == MOE_W_Q4_1) {
+                        const uint64_t s2 = sX2[col0 / 2 + j];
+                        accA[c][j] = fma2u(mA2, s2, accA[c][j]);
+                        accB[c][j] = fma2u(mB2, s2, accB[c][j]);
+                    }
                 }
             }
         }
@@ -629,24 +631,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (b == nb - 1) {
             // item complete: write this thread's row for every valid token
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float a[2], bb[2];
-                upk2(accA[j], a[0], a[1]);
-                upk2(accB[j], bb[0], bb[1]);
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int n = col0 + 2 * j + e;
-                    if (n < I.rows) {
-                        float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
-                        if (GU) {
-                            o[0] = silu_mul(a[e], bb[e]);
-                        } else {
-                            o[0] = a[e];
-                            o[BM] = bb[e];
+                for (int j = 0; j < 8; ++j) {
+                    float a[2], bb[2];
+                    upk2(accA[c][j], a[0], a[1]);
+                    upk2(accB[c][j], bb[0], bb[1]);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int n = h * 32 + c * 16 + 2 * j + e;
+                        if (n < I.rows) {
+                            float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
+                            if (GU) {
+                                o[0] = silu_mul(a[e], bb[e]);
+                            } else {
+                                o[0] = a[e];
+                                o[BM] = bb[e];
+                            }
                         }
                     }
+                    accA[c][j] = accB[c][j] = 0ull;
                 }
-                accA[j] = accB[j] = 0ull;
             }
         }
         return true;
@@ -656,23 +661,37 @@ __global__ void __launch_bounds__(THREADS, 1)
     // warp-uniform (__all_sync), so the warp-collective TMEM loads never see a
     // diverged warp; a failed MMA issue only raises the abort flag, which the
     // next waits observe.
-    bool ok = true;
-    if (is_producer) produce();
-    for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx) ok = convert(idx);
-    for (int idx = 0; idx < total && ok; ++idx) {
-        if (is_producer) produce();
-        if (is_mma) mma_try();
-        ok = epilogue(idx);
-        if (ok && idx + LOOKAHEAD < total) ok = convert(idx + LOOKAHEAD);
-    }
-    // every MMA must be issued before the CTA drains (thread 32 finishes the tail)
-    if (is_mma) {
-        long long t0 = clock64();
-        while (next_mma < total && !*abort_flag && clock64() - t0 < TIMEOUT_CYCLES) mma_try();
+    if (is_control) {
+        // lane 0 issues TMA stages and MMAs as their inputs become ready; the
+        // other lanes of this warp have nothing to do
+        if (lane == 0) {
+            long long t0 = clock64();
+            int last_next = -1, last_mma = -1;
+            while ((next_stage < total_stages || next_mma < total) && !*abort_flag) {
+                produce();
+                mma_try();
+                if (next_stage != last_next || next_mma != last_mma) {
+                    last_next = next_stage;
+                    last_mma = next_mma;
+                    t0 = clock64();
+                } else if (clock64() - t0 > TIMEOUT_CYCLES) {
+                    *abort_flag = 1;
+                } else {
+                    __nanosleep(32);
+                }
+            }
+        }
+    } else {
+        bool ok = true;
+        for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx) ok = convert(idx);
+        for (int idx = 0; idx < total && ok; ++idx) {
+            ok = epilogue(idx);
+            if (ok && idx + LOOKAHEAD < total) ok = convert(idx + LOOKAHEAD);
+        }
     }
 
     // drain what this CTA started before it may exit (only waits on the abort path)
-    if (is_producer) {
+    if (is_control && lane == 0) {
         for (int gs = (next_stage > RS ? next_stage - RS : 0); gs < next_stage; ++gs) {
             long long t0 = clock64();
             while (!mbar_try_wait(bar(B_RAW_FULL + gs % RS), (gs / RS) & 1) &&
@@ -680,7 +699,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     }
-    if (is_mma && next_mma > 0) {  // the last commit covers every MMA issued before it
+    if (is_control && lane == 0 && next_mma > 0) {  // the last commit covers every MMA before it
         const int last = next_mma - 1;
         long long t0 = clock64();
         while (!mbar_try_wait(bar(B_TM_FULL + last % NB), (last / NB) & 1) &&
