@@ -46,7 +46,7 @@ constexpr int RS = 2;        // raw stages
 constexpr int NB = 4;        // TMEM partial buffers (2 matrices x BN columns each)
 constexpr int NF = 4;        // fp16 operand slots = blocks converted ahead of the epilogue
 constexpr int NSC = 2 * NF;  // scale ring slots (a slot is reused 2*NF blocks later)
-constexpr int NWORK = 8;                      // worker warps (convert + epilogue)
+constexpr int NWORK = 16;                     // worker warps (convert + epilogue)
 constexpr int THREADS = 32 * (NWORK + 1);     // + one control warp (TMA and MMA issue)
 constexpr int NWARPS = NWORK;                 // consumer barriers count one arrival per worker warp
 constexpr int LOOKAHEAD = NF;
@@ -488,16 +488,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
 
     // ---- worker duty (warps 0 .. NWORK-1)
-    const int wt = threadIdx.x;     // 0..255 for workers
+    const int wt = threadIdx.x;     // 0..511 for workers
     const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int h = (warp >> 2) & 1;  // column half: tokens 32h .. 32h+31
+    const int g = (warp >> 2) & 3;  // column group: tokens 16g .. 16g+15
     const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
-    // accumulators: 2 chunks x 16 columns for each matrix, as 8 packed pairs
-    uint64_t accA[2][8], accB[2][8];
+    // accumulators: 16 columns for each matrix, as 8 packed pairs
+    uint64_t accA[8], accB[8];
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
+    for (int j = 0; j < 8; ++j) accA[j] = accB[j] = 0ull;
 
     auto convert = [&](int idx) -> bool {
         const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
@@ -510,9 +508,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         float* sc = (float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
         // weights: 256 rows x 32 values of block blk
         if (WT == MOE_W_Q8_0) {
-#pragma unroll
-            for (int rep = 0; rep < 2; ++rep) {
-                const int u = wt + rep * 256;             // 512 units of 16 values
+            {
+                const int u = wt;                         // 512 units of 16 values
                 const int R = u >> 1, hh = u & 1;
                 const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
                 const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
@@ -525,7 +522,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
                 *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
             }
-        } else {
+        } else if (wt < 2 * BM) {
             const int R = wt;                     // 256 units of 32 values
             const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
             const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
@@ -599,29 +596,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
         const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
         const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
+        const int col0 = g * 16;
+        if (col0 < I.ncols) {
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + tb * (2 * BN) + col0;
+            uint32_t ra[16], rb[16];
+            tmem_ld16(taddr, ra);
+            tmem_ld16(taddr + BN, rb);
+            uint64_t dxp[8];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int col0 = h * 32 + c * 16;
-            if (col0 < I.ncols) {
-                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + tb * (2 * BN) + col0;
-                uint32_t ra[16], rb[16];
-                tmem_ld16(taddr, ra);
-                tmem_ld16(taddr + BN, rb);
-                uint64_t dxp[8];
+            for (int j = 0; j < 8; ++j) dxp[j] = dX2[col0 / 2 + j];
+            tmem_wait32(ra, rb);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) dxp[j] = dX2[col0 / 2 + j];
-                tmem_wait32(ra, rb);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
-                    const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
-                    accA[c][j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[c][j]);
-                    accB[c][j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[c][j]);
-                    if (WT == MOE_W_Q4_1) {
-                        const uint64_t s2 = sX2[col0 / 2 + j];
-                        accA[c][j] = fma2u(mA2, s2, accA[c][j]);
-                        accB[c][j] = fma2u(mB2, s2, accB[c][j]);
-                    }
+            for (int j = 0; j < 8; ++j) {
+                const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
+                const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
+                accA[j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[j]);
+                accB[j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[j]);
+                if (WT == MOE_W_Q4_1) {
+                    const uint64_t s2 = sX2[col0 / 2 + j];
+                    accA[j] = fma2u(mA2, s2, accA[j]);
+                    accB[j] = fma2u(mB2, s2, accB[j]);
                 }
             }
         }
@@ -631,27 +625,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (b == nb - 1) {
             // item complete: write this thread's row for every valid token
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int j = 0; j < 8; ++j) {
+                float a[2], bb[2];
+                upk2(accA[j], a[0], a[1]);
+                upk2(accB[j], bb[0], bb[1]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float a[2], bb[2];
-                    upk2(accA[c][j], a[0], a[1]);
-                    upk2(accB[c][j], bb[0], bb[1]);
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int n = h * 32 + c * 16 + 2 * j + e;
-                        if (n < I.rows) {
-                            float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
-                            if (GU) {
-                                o[0] = silu_mul(a[e], bb[e]);
-                            } else {
-                                o[0] = a[e];
-                                o[BM] = bb[e];
-                            }
+                for (int e = 0; e < 2; ++e) {
+                    const int n = col0 + 2 * j + e;
+                    if (n < I.rows) {
+                        float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
+                        if (GU) {
+                            o[0] = silu_mul(a[e], bb[e]);
+                        } else {
+                            o[0] = a[e];
+                            o[BM] = bb[e];
                         }
                     }
-                    accA[c][j] = accB[c][j] = 0ull;
                 }
+                accA[j] = accB[j] = 0ull;
             }
         }
         return true;
