@@ -13,19 +13,19 @@
 // integer.  The per-block fp32 scaling then runs on the CUDA cores in the same
 // order as the scalar definition: acc = fma(dW*dx, I_b, acc) (+ fma(mW, sx, acc)).
 //
-// One persistent CTA of 16 warps per SM (static round-robin over the
+// One persistent CTA of 8 warps per SM (static round-robin over the
 // device-built, longest-first work list).  A work item is 128 tokens of one
 // expert times two 128-row weight blocks (gate and up rows j0..j0+127 for
 // stage 4; down rows i0..i0+255 for stage 6).  Every warp is a worker: for
 // 32-block b it reads its quarter of the TMEM lanes (its weight rows) for its
-// group of 32 columns (tokens), scales and accumulates in registers (64 fp32
-// per thread), then converts its share of block b+2's raw tiles into the fp16
-// operand layout.  Two threads carry extra duties: thread 0 issues the TMA loads of
+// half of the columns (tokens), scales and accumulates in registers (128 fp32
+// per thread), then converts block b+2's raw tiles into the fp16 operand
+// layout.  Two threads carry extra duties: thread 0 issues the TMA loads of
 // raw int8 / 4-bit tiles and fp16 scales (4 blocks a stage, never blocking),
 // thread 32 issues block b+1's MMAs -- 2 x (M=128, N<=128, K=16) per matrix --
 // into the TMEM buffer the workers are not reading, committed to an mbarrier.
-// (The register file is split over the four SM sub-partitions: 16 warps of up
-// to 128 registers fill it, four warps per sub-partition to hide latency.)
+// (The register file is split over the four SM sub-partitions, so 8 warps of
+// up to 255 registers fit where 10 warps of 200 would not.)
 // Every wait is bounded: on timeout the kernel sets MOE_DEV_ERR_TIMEOUT, drains
 // what it started and exits.
 #include <cudaTypedefs.h>
@@ -39,24 +39,21 @@
 namespace moe {
 namespace tc {
 
-constexpr int BN = 64;       // tokens per work item (TMEM columns per matrix)
+constexpr int BN = 128;      // tokens per work item (TMEM columns per matrix)
 constexpr int BM = 128;      // weight rows per matrix (TMEM lanes)
 constexpr int KBS = 4;       // 32-blocks per raw stage
-constexpr int RS = 2;        // raw stages
-constexpr int NB = 4;        // TMEM partial buffers (2 matrices x BN columns each)
-constexpr int NF = 4;        // fp16 operand slots = blocks converted ahead of the epilogue
-constexpr int NSC = 2 * NF;  // scale ring slots (a slot is reused 2*NF blocks later)
-constexpr int NWORK = 16;                     // worker warps (convert + epilogue)
-constexpr int THREADS = 32 * (NWORK + 1);     // + one control warp (TMA and MMA issue)
-constexpr int NWARPS = NWORK;                 // consumer barriers count one arrival per worker warp
-constexpr int LOOKAHEAD = NF;
+constexpr int RS = 3;        // raw stages
+constexpr int NF = 2;        // fp16 operand slots = TMEM partial buffers
+constexpr int NSC = 4;       // scale ring slots
+constexpr int THREADS = 256; // 8 warps, 2 per SM sub-partition
+constexpr int LOOKAHEAD = 2; // blocks converted ahead of the epilogue
 constexpr int ITEM_RING = 8; // work items kept in shared memory (written by the producer)
 constexpr long long TIMEOUT_CYCLES = 1LL << 32;
 
 constexpr int F16_A = 2 * BM * 64;  // two 128-row matrices x 32 fp16
 constexpr int F16_B = BN * 64;
 constexpr int F16_SLOT = F16_A + F16_B;
-constexpr int SC_SLOT = (2 * BM * 2 + BN * 2) * 4;  // dW, mW [256]; dX, sX [BN] (fp32)
+constexpr int SC_SLOT = (2 * BM * 2 + BN * 2) * 4;  // dW, mW [256]; dX, sX [128] (fp32)
 
 __host__ __device__ constexpr int cround(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -78,7 +75,7 @@ struct Lay {
     static constexpr int O_F16 = RS * STAGE;
     static constexpr int O_SC = O_F16 + NF * F16_SLOT;
     static constexpr int O_BAR = O_SC + NSC * SC_SLOT;
-    static constexpr int N_BARS = 2 * RS + NF + 2 * NB;
+    static constexpr int N_BARS = 2 * RS + 3 * NF;
     static constexpr int O_ITEMS = cround(O_BAR + N_BARS * 8 + 16, 16);
     static constexpr int SMEM = O_ITEMS + ITEM_RING * 16 + 1024;  // + alignment slack
 };
@@ -366,7 +363,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int B_RAW_FULL = 0, B_RAW_EMPTY = RS, B_F16_FULL = 2 * RS, B_TM_FULL = 2 * RS + NF,
-              B_TM_EMPTY = 2 * RS + NF + NB;
+              B_TM_EMPTY = 2 * RS + 2 * NF;
 
     const int n_items = *P.n_tiles * P.mt_count;
     if ((int)blockIdx.x >= n_items) return;
@@ -376,17 +373,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int total = my_items * nb;
     const int total_stages = my_items * spi;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool is_control = warp == NWORK;  // the last warp issues TMA loads and MMAs
+    const bool is_producer = threadIdx.x == 0;
+    const bool is_mma = threadIdx.x == 32;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
             mbar_init(bar(B_RAW_FULL + i), 1);
-            mbar_init(bar(B_RAW_EMPTY + i), NWARPS);
+            mbar_init(bar(B_RAW_EMPTY + i), THREADS / 32);
         }
-        for (int i = 0; i < NF; ++i) mbar_init(bar(B_F16_FULL + i), NWARPS);
-        for (int i = 0; i < NB; ++i) {
+        for (int i = 0; i < NF; ++i) {
+            mbar_init(bar(B_F16_FULL + i), THREADS / 32);
             mbar_init(bar(B_TM_FULL + i), 1);
-            mbar_init(bar(B_TM_EMPTY + i), NWARPS);
+            mbar_init(bar(B_TM_EMPTY + i), THREADS / 32);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -446,39 +444,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             ++next_stage;
         }
     };
-    // ---- MMA duty (thread 32): issue, in order, every block whose fp16 operands
-    // are complete and whose TMEM buffer (idx % NB) has been drained; never blocks.
-    int next_mma = 0;
-    auto mma_try = [&]() {
-        while (next_mma < total) {
-            const int idx = next_mma;
-            const int fs = idx % NF, tb = idx % NB;
-            if (!mbar_test_wait(bar(B_F16_FULL + fs), (idx / NF) & 1)) return;
-            if (idx >= NB && !mbar_test_wait(bar(B_TM_EMPTY + tb), ((idx / NB) - 1) & 1)) return;
-            tc_fence_after();
-            const Item I = item(idx / nb);  // ordered by the f16_full barrier
-            const uint32_t fa = sbase + L::O_F16 + fs * F16_SLOT;
-            const uint32_t fbB = fa + F16_A;
-            const uint32_t id = idesc_f16(BM, I.ncols);
-#pragma unroll
-            for (int mat = 0; mat < 2; ++mat) {
-#pragma unroll
-                for (int k16 = 0; k16 < 2; ++k16) {
-                    mma_f16(tmem + tb * (2 * BN) + mat * BN,
-                            sdesc(fa + mat * (BM * 64) + k16 * 256, 128, 512),
-                            sdesc(fbB + k16 * 256, 128, 512), id, (uint32_t)k16);
-                }
-            }
-            mma_commit(bar(B_TM_FULL + tb));
-            ++next_mma;
-        }
-    };
-    // bounded wait of a worker thread (sleeps in hardware between probes)
+    // bounded wait; thread 0 keeps producing while it waits, the others sleep
     auto waitp = [&](uint32_t b, uint32_t parity) -> bool {
         if (mbar_test_wait(b, parity)) return true;
         long long t0 = clock64();
         while (true) {
-            if (mbar_try_wait_sleep(b, parity)) return true;
+            if (is_producer) {
+                produce();
+                if (mbar_test_wait(b, parity)) return true;
+            } else if (mbar_try_wait_sleep(b, parity)) {
+                return true;
+            }
             if (*abort_flag) return false;
             if (clock64() - t0 > TIMEOUT_CYCLES) {
                 *abort_flag = 1;
@@ -487,15 +463,41 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     };
 
-    // ---- worker duty (warps 0 .. NWORK-1)
-    const int wt = threadIdx.x;     // 0..511 for workers
-    const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int g = (warp >> 2) & 3;  // column group: tokens 16g .. 16g+15
-    const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
-    // accumulators: 16 columns for each matrix, as 8 packed pairs
-    uint64_t accA[8], accB[8];
+    // ---- MMA duty (thread 32): block idx's products into TMEM buffer idx % 2.
+    int mma_issued = 0;
+    auto issue_mma = [&](int idx) -> bool {
+        const int sl = idx % NF, u = idx / NF;
+        if (!waitp(bar(B_F16_FULL + sl), u & 1)) return false;
+        if (u > 0 && !waitp(bar(B_TM_EMPTY + sl), (u - 1) & 1)) return false;
+        tc_fence_after();
+        const Item I = item(idx / nb);  // read after the barrier that orders it
+        const uint32_t fa = sbase + L::O_F16 + sl * F16_SLOT;
+        const uint32_t fbB = fa + F16_A;
+        const uint32_t id = idesc_f16(BM, I.ncols);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) accA[j] = accB[j] = 0ull;
+        for (int mat = 0; mat < 2; ++mat) {
+#pragma unroll
+            for (int k16 = 0; k16 < 2; ++k16) {
+                mma_f16(tmem + sl * 256 + mat * 128, sdesc(fa + mat * (BM * 64) + k16 * 256, 128, 512),
+                        sdesc(fbB + k16 * 256, 128, 512), id, (uint32_t)k16);
+            }
+        }
+        mma_commit(bar(B_TM_FULL + sl));
+        mma_issued = idx + 1;
+        return true;
+    };
+
+    // ---- worker duty (all threads)
+    const int wt = threadIdx.x;     // 0..255
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int h = warp >> 2;        // column half
+    const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
+    // accumulators: 4 chunks x 16 columns for each matrix, as 8 packed pairs
+    uint64_t accA[4][8], accB[4][8];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
 
     auto convert = [&](int idx) -> bool {
         const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
@@ -508,9 +510,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         float* sc = (float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
         // weights: 256 rows x 32 values of block blk
         if (WT == MOE_W_Q8_0) {
-            {
-                const int u = wt;                         // 512 units of 16 values
-                const int R = u >> 1, hh = u & 1;
+#pragma unroll
+            for (int rep = 0; rep < 2; ++rep) {
+                // lanes 0-7 take 8 consecutive rows, lanes 8-15 their second
+                // halves, lanes 16-31 the next 8 rows: every 8-lane phase of the
+                // 16-byte loads and stores touches 8 distinct bank groups
+                const int R = rep * 128 + (wt >> 5) * 16 + (lane & 7) + 8 * (lane >> 4);
+                const int hh = (lane >> 3) & 1;
                 const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
                 const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
                 uint4 o0, o1;
@@ -522,8 +528,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
                 *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
             }
-        } else if (wt < 2 * BM) {
-            const int R = wt;                     // 256 units of 32 values
+        } else {
+            const int R = wt;
             const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
             const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -537,7 +543,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         // activations: ncols rows x 32 values, units of 16
         if (wt < 2 * I.ncols) {
-            const int n = wt >> 1, hh = wt & 1;
+            const int n = (wt >> 5) * 16 + (lane & 7) + 8 * (lane >> 4);  // as for the weights
+            const int hh = (lane >> 3) & 1;
             const int ch = (blk * 2 + hh) ^ (n & 7);
             const uint4 v = *(const uint4*)(st + L::O_X + n * 128 + ch * 16);
             uint4 o0, o1;
@@ -557,7 +564,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             *(uint4*)(fbB + f16_off(n, 2 * hh + 1)) = o1;
         }
         // scales of block blk as fp32: dW[256], mW[256], dX[128], sX[128]
-        if (wt < 2 * BM) {
+        {
             const int R = wt;
             const int si = GU ? (((R >> 7) * KBS + blk) * BM + (R & 127)) : (blk * 2 * BM + R);
             sc[R] = __half2float(((const __half*)(st + L::O_WS))[si]);
@@ -569,7 +576,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         // make this thread's fp16 operands visible to the tensor core, then one
-        // arrival per warp (an mbarrier is a single word: 512 arrivals serialize)
+        // arrival per warp (an mbarrier is a single word)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
@@ -581,9 +588,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     auto epilogue = [&](int idx) -> bool {
         const int i = idx / nb, b = idx - i * nb;
-        const int tb = idx % NB;
+        const int sl = idx % NF;
         // warp-uniform decision: the TMEM loads below are warp-collective
-        if (!__all_sync(0xffffffffu, waitp(bar(B_TM_FULL + tb), (idx / NB) & 1))) return false;
+        if (!__all_sync(0xffffffffu, waitp(bar(B_TM_FULL + sl), (idx / NF) & 1))) return false;
         tc_fence_after();
         const Item I = item(i);
         const float* sc = (const float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
@@ -596,53 +603,75 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
         const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
         const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
-        const int col0 = g * 16;
-        if (col0 < I.ncols) {
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + tb * (2 * BN) + col0;
-            uint32_t ra[16], rb[16];
-            tmem_ld16(taddr, ra);
-            tmem_ld16(taddr + BN, rb);
-            uint64_t dxp[8];
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + sl * 256;
+        const int nch = min(4, max(0, (I.ncols - h * 64) / 16));  // active 16-column chunks
+        // software pipeline: chunk c+1's TMEM loads (and scales) are in flight
+        // while chunk c is scaled and accumulated
+        uint32_t ra[2][16], rb[2][16];
+        uint64_t dxp[8];
+        if (nch > 0) {
+            tmem_ld16(tbase + h * 64, ra[0]);
+            tmem_ld16(tbase + 128 + h * 64, rb[0]);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dxp[j] = dX2[col0 / 2 + j];
-            tmem_wait32(ra, rb);
+            for (int j = 0; j < 8; ++j) dxp[j] = dX2[h * 32 + j];
+            tmem_wait32(ra[0], rb[0]);
+        }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
-                const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
-                accA[j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[j]);
-                accB[j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[j]);
-                if (WT == MOE_W_Q4_1) {
-                    const uint64_t s2 = sX2[col0 / 2 + j];
-                    accA[j] = fma2u(mA2, s2, accA[j]);
-                    accB[j] = fma2u(mB2, s2, accB[j]);
+        for (int c = 0; c < 4; ++c) {
+            if (c < nch) {
+                const int cur = c & 1, nxt = cur ^ 1;
+                const int col0 = h * 64 + c * 16;
+                if (c + 1 < nch) {
+                    tmem_ld16(tbase + col0 + 16, ra[nxt]);
+                    tmem_ld16(tbase + 128 + col0 + 16, rb[nxt]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint64_t pa = pk2(ra[cur][2 * j], ra[cur][2 * j + 1]);
+                    const uint64_t pb = pk2(rb[cur][2 * j], rb[cur][2 * j + 1]);
+                    accA[c][j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[c][j]);
+                    accB[c][j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[c][j]);
+                    if (WT == MOE_W_Q4_1) {
+                        const uint64_t s2 = sX2[col0 / 2 + j];
+                        accA[c][j] = fma2u(mA2, s2, accA[c][j]);
+                        accB[c][j] = fma2u(mB2, s2, accB[c][j]);
+                    }
+                }
+                if (c + 1 < nch) {
+                    // next chunk's scales load while its TMEM loads complete
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) dxp[j] = dX2[(col0 + 16) / 2 + j];
+                    tmem_wait32(ra[nxt], rb[nxt]);
                 }
             }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_TM_EMPTY + tb));
+        if (lane == 0) mbar_arrive(bar(B_TM_EMPTY + sl));
         if (b == nb - 1) {
             // item complete: write this thread's row for every valid token
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float a[2], bb[2];
-                upk2(accA[j], a[0], a[1]);
-                upk2(accB[j], bb[0], bb[1]);
+            for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int n = col0 + 2 * j + e;
-                    if (n < I.rows) {
-                        float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
-                        if (GU) {
-                            o[0] = silu_mul(a[e], bb[e]);
-                        } else {
-                            o[0] = a[e];
-                            o[BM] = bb[e];
+                for (int j = 0; j < 8; ++j) {
+                    float a[2], bb[2];
+                    upk2(accA[c][j], a[0], a[1]);
+                    upk2(accB[c][j], bb[0], bb[1]);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int n = h * 64 + c * 16 + 2 * j + e;
+                        if (n < I.rows) {
+                            float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
+                            if (GU) {
+                                o[0] = silu_mul(a[e], bb[e]);
+                            } else {
+                                o[0] = a[e];
+                                o[BM] = bb[e];
+                            }
                         }
                     }
+                    accA[c][j] = accB[c][j] = 0ull;
                 }
-                accA[j] = accB[j] = 0ull;
             }
         }
         return true;
@@ -652,37 +681,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     // warp-uniform (__all_sync), so the warp-collective TMEM loads never see a
     // diverged warp; a failed MMA issue only raises the abort flag, which the
     // next waits observe.
-    if (is_control) {
-        // lane 0 issues TMA stages and MMAs as their inputs become ready; the
-        // other lanes of this warp have nothing to do
-        if (lane == 0) {
-            long long t0 = clock64();
-            int last_next = -1, last_mma = -1;
-            while ((next_stage < total_stages || next_mma < total) && !*abort_flag) {
-                produce();
-                mma_try();
-                if (next_stage != last_next || next_mma != last_mma) {
-                    last_next = next_stage;
-                    last_mma = next_mma;
-                    t0 = clock64();
-                } else if (clock64() - t0 > TIMEOUT_CYCLES) {
-                    *abort_flag = 1;
-                } else {
-                    __nanosleep(32);
-                }
-            }
-        }
-    } else {
-        bool ok = true;
-        for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx) ok = convert(idx);
-        for (int idx = 0; idx < total && ok; ++idx) {
-            ok = epilogue(idx);
-            if (ok && idx + LOOKAHEAD < total) ok = convert(idx + LOOKAHEAD);
-        }
+    bool ok = true;
+    if (is_producer) produce();
+    for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx)
+        ok = convert(idx);
+    if (ok && is_mma) issue_mma(0);
+    for (int idx = 0; idx < total && ok; ++idx) {
+        if (is_producer) produce();
+        if (is_mma && idx + 1 < total) issue_mma(idx + 1);
+        ok = epilogue(idx);
+        if (ok && idx + LOOKAHEAD < total) ok = convert(idx + LOOKAHEAD);
     }
 
     // drain what this CTA started before it may exit (only waits on the abort path)
-    if (is_control && lane == 0) {
+    if (is_producer) {
         for (int gs = (next_stage > RS ? next_stage - RS : 0); gs < next_stage; ++gs) {
             long long t0 = clock64();
             while (!mbar_try_wait(bar(B_RAW_FULL + gs % RS), (gs / RS) & 1) &&
@@ -690,10 +702,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     }
-    if (is_control && lane == 0 && next_mma > 0) {  // the last commit covers every MMA before it
-        const int last = next_mma - 1;
+    if (is_mma && mma_issued > 0) {
+        const int last = mma_issued - 1;
         long long t0 = clock64();
-        while (!mbar_try_wait(bar(B_TM_FULL + last % NB), (last / NB) & 1) &&
+        while (!mbar_try_wait(bar(B_TM_FULL + last % NF), (last / NF) & 1) &&
                clock64() - t0 < TIMEOUT_CYCLES) {
         }
     }
