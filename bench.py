@@ -186,6 +186,24 @@ def layer_accounting(cfg, n_active: int, rec_bytes: int, R: int):
     return stages, total_bytes, ops
 
 
+# ------------------------------------------------------------ multi-rank --
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The slowest rank's time is the job's time: all-reduce MAX of a per-rank
+    scalar (a no-op on one rank)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank runs its own replica of the workload."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 # -------------------------------------------------------------- GPU arm --
 
 def run_gpu(args, rank, world, local_rank):
@@ -264,11 +282,7 @@ def run_gpu(args, rank, world, local_rank):
     clocks = sampler.stop() if sampler else None
     stage_ms = np.array([[ev[i].elapsed_time(ev[i + 1]) for i in range(7)] for ev in events])
     step_ms = stage_ms.sum(axis=1)
-    ms = float(step_ms.mean())
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(step_ms.mean()), dist, dev)
 
     # end to end through the public API: pinned host inputs in, output out
     hx = torch.from_numpy(wl.x).pin_memory()
@@ -299,11 +313,7 @@ def run_gpu(args, rank, world, local_rank):
         b.record(stream)
         torch.cuda.synchronize(dev)
         e_ms.append(a.elapsed_time(b))
-    e2e_ms = float(np.mean(e_ms))
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(float(np.mean(e_ms)), dist, dev)
     assert m.moe_device_error(layer.ws) == 0
 
     if rank != 0:
@@ -329,7 +339,7 @@ def run_gpu(args, rank, world, local_rank):
     t_roof = max(total_bytes / (hbm * 1e9), ops / (tflops * 1e12))
     qs_sec = mean_stage[1] / 1e3
     qs_gbs = stages["quantize_scatter"][1] / qs_sec / 1e9
-    value = world * T / (ms / 1e3)
+    value = weak_scaling_value(world, T, ms)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -356,7 +366,7 @@ def run_gpu(args, rank, world, local_rank):
         "quantize_scatter": {"GB/s": round(qs_gbs, 1), "frac_of_hbm": round(qs_gbs / hbm, 4),
                              "bytes": int(stages["quantize_scatter"][1])},
         "phases_ms": phases,
-        "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(weak_scaling_value(world, T, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": int(wl.x.nbytes + wl.ids.nbytes + wl.w.nbytes),
                 "d2h_bytes_per_step": int(T * d * 4)},
