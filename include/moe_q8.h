@@ -206,6 +206,33 @@ int moe_grouped_mmq_down(int wtype, const uint8_t* group_base, size_t slot_strid
 int moe_combine_topk(const float* y, int R, const int32_t* slot, const float* w, int T, int K,
                      int d, float* out, void* stream);
 
+/*
+ * Stage 1 without a workspace.  The pull-request pages have no counterpart of
+ * this call; it exists for callers that cannot allocate device memory and so
+ * cannot hand the library a workspace -- for example code embedded in a host
+ * framework that owns every device allocation, or code that must not trigger
+ * cudaMalloc's implicit device synchronization.  It computes exactly what
+ * moe_build_slot_map computes (same arguments without ws / ws_bytes) and
+ * allocates nothing: its scratch is a file-scope device array of 1 MiB + 256 B
+ * that every GPU which loads the library holds until the process exits, and it
+ * calls no cudaMalloc or cudaFree.
+ *   - Limit: ceil(T*K / 1024) * E <= 262144 (the per-chunk expert counts must
+ *     fit the array), e.g. T*K <= 262144 at E = 1024 or T*K <= 524288 at E = 512;
+ *     larger sizes return MOE_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array, which keeps the previous call's
+ *     contents: each call clears its header first, and calls that overlap on
+ *     the GPU (other streams, or other threads' calls on this device) race --
+ *     run them one after another.
+ *   - Ids outside [0, E) are dropped (slot -1) as in moe_build_slot_map; the
+ *     error word is not reported.
+ */
+int moe_build_slot_map_noalloc(const int32_t* ids, int T, int K, int E, int32_t* offsets,
+                               int32_t* slot, int32_t* src, int32_t* active, int32_t* n_active,
+                               void* stream);
+
 /* Synchronize `stream`, read the workspace error word into *bits (host) and
    clear it.  Returns MOE_ERR_DEVICE if any bit was set, MOE_OK otherwise. */
 int moe_device_error(void* ws, uint32_t* bits, void* stream);

@@ -49,6 +49,7 @@ _SIGNATURES = {
     "moe_requant_hidden_q8_1": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_grouped_mmq_down": (_I, [_I, _P, _Z, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_combine_topk": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_build_slot_map_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_launch_count": (ctypes.c_ulonglong, []),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -194,6 +195,17 @@ def moe_combine_topk(y, R, slot, w, T, K, d, out, stream=None):
     _dev(y, slot, w, out)
     _check(lib().moe_combine_topk(_p(y), R, _p(slot), _p(w), T, K, d, _p(out), _s(stream)),
            "moe_combine_topk")
+
+
+def moe_build_slot_map_noalloc(ids, E, offsets, slot, src, active, n_active, stream=None):
+    """moe_build_slot_map without a workspace, for callers that cannot allocate
+    device memory: the scratch is a fixed device array inside the library (see
+    include/moe_q8.h for its limit and its once-per-device set-up)."""
+    _dev(ids, offsets, slot, src, active, n_active)
+    T, K = ids.shape
+    _check(lib().moe_build_slot_map_noalloc(_p(ids), T, K, E, _p(offsets), _p(slot), _p(src),
+                                            _p(active), _p(n_active), _s(stream)),
+           "moe_build_slot_map_noalloc")
 
 
 def moe_device_error(ws, stream=None) -> int:
