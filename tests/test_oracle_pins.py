@@ -488,3 +488,18 @@ def test_layer_end_to_end_tiny(wtype):
             continue
         rel = np.linalg.norm(r["out"][t] - ref[t]) / np.linalg.norm(ref[t])
         assert rel < 0.05, (t, rel)
+
+
+def test_requant_hidden_uses_the_golden_quantizer():
+    """Stage a5 quantizes each 32-block of a hidden row exactly like the golden
+    hand-derived blocks (identity row map, one row per case)."""
+    cases = _golden_blocks()
+    h = np.stack([c["x"] for c in cases]).astype(np.float32)
+    h = np.concatenate([h, h[::-1]], axis=1)  # two blocks per row
+    hq, hds = oracle.requant_hidden_q8_1(h)
+    for i, c in enumerate(cases):
+        assert np.array_equal(hq[i, :32], c["q"])
+        assert hds[i, 0, 0] == c["d"] and hds[i, 0, 1] == c["s"]
+        j = len(cases) - 1 - i
+        assert np.array_equal(hq[j, 32:], c["q"])
+        assert hds[j, 1, 0] == c["d"] and hds[j, 1, 1] == c["s"]
