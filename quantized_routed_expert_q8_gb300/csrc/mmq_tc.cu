@@ -13,19 +13,22 @@
 // integer.  The per-block fp32 scaling then runs on the CUDA cores in the same
 // order as the scalar definition: acc = fma(dW*dx, I_b, acc) (+ fma(mW, sx, acc)).
 //
-// One persistent CTA of 8 warps per SM (static round-robin over the
+// One persistent CTA of 16 warps per SM (static round-robin over the
 // device-built, longest-first work list).  A work item is 128 tokens of one
 // expert times two 128-row weight blocks (gate and up rows j0..j0+127 for
-// stage 4; down rows i0..i0+255 for stage 6).  Every warp is a worker: for
-// 32-block b it reads its quarter of the TMEM lanes (its weight rows) for its
-// half of the columns (tokens), scales and accumulates in registers (128 fp32
-// per thread), then converts block b+2's raw tiles into the fp16 operand
-// layout.  Two threads carry extra duties: thread 0 issues the TMA loads of
-// raw int8 / 4-bit tiles and fp16 scales (4 blocks a stage, never blocking),
-// thread 32 issues block b+1's MMAs -- 2 x (M=128, N<=128, K=16) per matrix --
-// into the TMEM buffer the workers are not reading, committed to an mbarrier.
-// (The register file is split over the four SM sub-partitions, so 8 warps of
-// up to 255 registers fit where 10 warps of 200 would not.)
+// stage 4; down rows i0..i0+255 for stage 6).  The warps split into roles, one
+// warpgroup each, connected by mbarrier full/empty rings:
+//   producer (warp 12): TMA loads of raw int8 / 4-bit tiles and fp16 scales,
+//     4 blocks a stage;
+//   converters (warps 8-11): raw tiles -> fp16 operands in the K-major layout
+//     the MMA descriptors read, fp16 scales -> fp32;
+//   MMA issuer (warp 13): 2 x (M=128, N<=128, K=16) per matrix into one of two
+//     TMEM buffers, committed to an mbarrier;
+//   epilogue (warps 0-7): warp w reads TMEM lane quarter w % 4 (its weight rows)
+//     for column half w / 4 (tokens), scales and accumulates in registers
+//     (128 fp32 per thread) and writes the item's outputs.
+// setmaxnreg moves registers from the converter/producer warpgroups to the
+// epilogue warpgroups.
 // Every wait is bounded: on timeout the kernel sets MOE_DEV_ERR_TIMEOUT, drains
 // what it started and exits.
 #include <cudaTypedefs.h>
@@ -43,12 +46,30 @@ constexpr int BN = 128;      // tokens per work item (TMEM columns per matrix)
 constexpr int BM = 128;      // weight rows per matrix (TMEM lanes)
 constexpr int KBS = 4;       // 32-blocks per raw stage
 constexpr int RS = 3;        // raw stages
-constexpr int NF = 2;        // fp16 operand slots = TMEM partial buffers
-constexpr int NSC = 4;       // scale ring slots
-constexpr int THREADS = 256; // 8 warps, 2 per SM sub-partition
-constexpr int LOOKAHEAD = 2; // blocks converted ahead of the epilogue
+constexpr int NFS = 2;       // fp16 operand slots
+constexpr int NTB = 2;       // TMEM partial buffers (256 columns each)
+constexpr int NSC = 4;       // fp32 scale slots
 constexpr int ITEM_RING = 8; // work items kept in shared memory (written by the producer)
 constexpr long long TIMEOUT_CYCLES = 1LL << 32;
+
+// Warp roles, one warpgroup each (a warpgroup puts one warp on every SM
+// sub-partition): warpgroups 0-1 scale and accumulate the block partials
+// (epilogue), warpgroup 2 converts raw tiles into fp16 operands and fp32
+// scales, warpgroup 3 holds the TMA producer (warp 12) and the MMA issuer
+// (warp 13).
+constexpr int EPI_WARPS = 8;
+constexpr int CVT_WARPS = 4;
+constexpr int THREADS = 512;
+// Register split.  The launch gives every thread LAUNCH_REGS; warpgroups 2-3
+// give registers back (setmaxnreg.dec) and warpgroups 0-1 take them
+// (setmaxnreg.inc), so both the CTA's total and every sub-partition's share
+// stay as launched.
+constexpr int LAUNCH_REGS = 128;  // 65536 / 512
+constexpr int EPI_REGS = 224;
+constexpr int CVT_REGS = 40;
+constexpr int AUX_REGS = 24;
+static_assert(2 * EPI_REGS + CVT_REGS + AUX_REGS == 4 * LAUNCH_REGS, "register split must balance");
+static_assert(THREADS * LAUNCH_REGS <= 65536, "launch registers exceed the register file");
 
 constexpr int F16_A = 2 * BM * 64;  // two 128-row matrices x 32 fp16
 constexpr int F16_B = BN * 64;
@@ -73,9 +94,9 @@ struct Lay {
     static constexpr int STAGE = cround(O_XS + XS_RAW, 1024);
     static constexpr uint32_t TX = W_RAW + X_RAW + WS_RAW + WM_RAW + XS_RAW;
     static constexpr int O_F16 = RS * STAGE;
-    static constexpr int O_SC = O_F16 + NF * F16_SLOT;
+    static constexpr int O_SC = O_F16 + NFS * F16_SLOT;
     static constexpr int O_BAR = O_SC + NSC * SC_SLOT;
-    static constexpr int N_BARS = 2 * RS + 3 * NF;
+    static constexpr int N_BARS = 2 * (RS + NFS + NSC + NTB);
     static constexpr int O_ITEMS = cround(O_BAR + N_BARS * 8 + 16, 16);
     static constexpr int SMEM = O_ITEMS + ITEM_RING * 16 + 1024;  // + alignment slack
 };
@@ -362,8 +383,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t* tmem_slot = (uint32_t*)(smem + L::O_BAR + L::N_BARS * 8);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
-    const int B_RAW_FULL = 0, B_RAW_EMPTY = RS, B_F16_FULL = 2 * RS, B_TM_FULL = 2 * RS + NF,
-              B_TM_EMPTY = 2 * RS + 2 * NF;
+    // full/empty pairs: raw stages (TMA -> converters), fp16 operands
+    // (converters -> MMA), fp32 scales (converters -> epilogue), TMEM partials
+    // (MMA -> epilogue)
+    constexpr int B_RAW_FULL = 0, B_RAW_EMPTY = RS;
+    constexpr int B_F16_FULL = 2 * RS, B_F16_EMPTY = B_F16_FULL + NFS;
+    constexpr int B_SC_FULL = B_F16_EMPTY + NFS, B_SC_EMPTY = B_SC_FULL + NSC;
+    constexpr int B_TM_FULL = B_SC_EMPTY + NSC, B_TM_EMPTY = B_TM_FULL + NTB;
 
     const int n_items = *P.n_tiles * P.mt_count;
     if ((int)blockIdx.x >= n_items) return;
@@ -373,18 +399,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int total = my_items * nb;
     const int total_stages = my_items * spi;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool is_producer = threadIdx.x == 0;
-    const bool is_mma = threadIdx.x == 32;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
             mbar_init(bar(B_RAW_FULL + i), 1);
-            mbar_init(bar(B_RAW_EMPTY + i), THREADS / 32);
+            mbar_init(bar(B_RAW_EMPTY + i), CVT_WARPS);
         }
-        for (int i = 0; i < NF; ++i) {
-            mbar_init(bar(B_F16_FULL + i), THREADS / 32);
+        for (int i = 0; i < NFS; ++i) {
+            mbar_init(bar(B_F16_FULL + i), CVT_WARPS);
+            mbar_init(bar(B_F16_EMPTY + i), 1);
+        }
+        for (int i = 0; i < NSC; ++i) {
+            mbar_init(bar(B_SC_FULL + i), CVT_WARPS);
+            mbar_init(bar(B_SC_EMPTY + i), EPI_WARPS);
+        }
+        for (int i = 0; i < NTB; ++i) {
             mbar_init(bar(B_TM_FULL + i), 1);
-            mbar_init(bar(B_TM_EMPTY + i), THREADS / 32);
+            mbar_init(bar(B_TM_EMPTY + i), EPI_WARPS);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -400,13 +431,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // ---- producer duty (thread 0): issue every raw stage whose slot is free.
-    // Never blocks; called at each step and from inside thread 0's waits.
-    int next_stage = 0;
     int4* ring = (int4*)(smem + L::O_ITEMS);
-    // item i as (slot, first row, valid rows, first weight row); written by thread 0
-    // before the first TMA of the item, read by everyone after a barrier that
-    // orders them after that TMA
+    // item i as (slot, first row, valid rows, first weight row); written by the
+    // producer before the first TMA of the item, read by the other roles after a
+    // barrier that orders them after that TMA
     auto item = [&](int i) -> Item {
         const int4 v = ring[i % ITEM_RING];
         Item I;
@@ -417,298 +445,305 @@ __global__ void __launch_bounds__(THREADS, 1)
         I.w0 = v.w;
         return I;
     };
-    auto produce = [&]() {
-        while (next_stage < total_stages) {
-            const int gs = next_stage, sl = gs % RS, u = gs / RS;
-            if (u > 0 && !mbar_test_wait(bar(B_RAW_EMPTY + sl), (u - 1) & 1)) return;
-            const int i = gs / spi, s = gs - i * spi;
-            if (s == 0) {
-                const Item J = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
-                ring[i % ITEM_RING] = make_int4(J.p, J.r0, J.rows, J.w0);
+    // bounded wait for a whole warp; the threads may sleep in hardware until the
+    // phase completes.  The result is warp-uniform.
+    auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
+        bool done = mbar_test_wait(b, parity);
+        if (!done) {
+            long long t0 = clock64();
+            while (true) {
+                if (mbar_try_wait_sleep(b, parity)) {
+                    done = true;
+                    break;
+                }
+                if (*abort_flag) break;
+                if (clock64() - t0 > TIMEOUT_CYCLES) {
+                    *abort_flag = 1;
+                    break;
+                }
             }
+        }
+        return __all_sync(0xffffffffu, done);
+    };
+
+    if (warp < EPI_WARPS) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
+        // ---- epilogue: for block idx, warp w reads TMEM lane quarter w % 4 (its
+        // 32 weight rows) for column half w / 4 (64 tokens) of both matrices,
+        // scales and accumulates in registers
+        const int q = warp & 3;         // TMEM lane quarter this warp may access
+        const int h = warp >> 2;        // column half
+        const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
+        // accumulators: 4 chunks x 16 columns for each matrix, as 8 packed pairs
+        uint64_t accA[4][8], accB[4][8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
+        for (int idx = 0; idx < total; ++idx) {
+            const int i = idx / nb, b = idx - i * nb;
+            const int tb = idx % NTB, ss = idx % NSC;
+            // warp-uniform decisions: the TMEM loads below are warp-collective
+            if (!wait_warp(bar(B_TM_FULL + tb), (idx / NTB) & 1)) break;
+            if (!wait_warp(bar(B_SC_FULL + ss), (idx / NSC) & 1)) break;
+            tc_fence_after();
             const Item I = item(i);
-            const uint32_t st = sbase + sl * L::STAGE;
-            const uint32_t fb = bar(B_RAW_FULL + sl);
-            mbar_expect_tx(fb, L::TX);
-            if (GU) {
-                tma_4d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, 0, I.p);
-                tma_4d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, 0, I.p);
-                if (WT == MOE_W_Q4_1) tma_4d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, 0, I.p);
-            } else {
-                tma_3d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, I.p);
-                tma_3d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, I.p);
-                if (WT == MOE_W_Q4_1) tma_3d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, I.p);
+            const float* sc = (const float*)(smem + L::O_SC + ss * SC_SLOT);
+            const float dA = sc[m], dB = sc[BM + m];
+            const float mA = WT == MOE_W_Q4_1 ? sc[2 * BM + m] : 0.0f;
+            const float mB = WT == MOE_W_Q4_1 ? sc[3 * BM + m] : 0.0f;
+            const uint64_t dA2 = pk2(__float_as_uint(dA), __float_as_uint(dA));
+            const uint64_t dB2 = pk2(__float_as_uint(dB), __float_as_uint(dB));
+            const uint64_t mA2 = pk2(__float_as_uint(mA), __float_as_uint(mA));
+            const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
+            const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
+            const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + tb * 256;
+            const int nch = min(4, max(0, (I.ncols - h * 64) / 16));  // active 16-column chunks
+            // software pipeline: chunk c+1's TMEM loads (and scales) are in flight
+            // while chunk c is scaled and accumulated
+            uint32_t ra[2][16], rb[2][16];
+            if (nch > 0) {
+                tmem_ld16(tbase + h * 64, ra[0]);
+                tmem_ld16(tbase + 128 + h * 64, rb[0]);
+                tmem_wait32(ra[0], rb[0]);
             }
-            tma_2d(&mX, fb, st + L::O_X, s * 128, I.r0);
-            tma_2d(&mXs, fb, st + L::O_XS, s * KBS, I.r0);
-            ++next_stage;
-        }
-    };
-    // bounded wait; thread 0 keeps producing while it waits, the others sleep
-    auto waitp = [&](uint32_t b, uint32_t parity) -> bool {
-        if (mbar_test_wait(b, parity)) return true;
-        long long t0 = clock64();
-        while (true) {
-            if (is_producer) {
-                produce();
-                if (mbar_test_wait(b, parity)) return true;
-            } else if (mbar_try_wait_sleep(b, parity)) {
-                return true;
-            }
-            if (*abort_flag) return false;
-            if (clock64() - t0 > TIMEOUT_CYCLES) {
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    };
-
-    // ---- MMA duty (thread 32): block idx's products into TMEM buffer idx % 2.
-    int mma_issued = 0;
-    auto issue_mma = [&](int idx) -> bool {
-        const int sl = idx % NF, u = idx / NF;
-        if (!waitp(bar(B_F16_FULL + sl), u & 1)) return false;
-        if (u > 0 && !waitp(bar(B_TM_EMPTY + sl), (u - 1) & 1)) return false;
-        tc_fence_after();
-        const Item I = item(idx / nb);  // read after the barrier that orders it
-        const uint32_t fa = sbase + L::O_F16 + sl * F16_SLOT;
-        const uint32_t fbB = fa + F16_A;
-        const uint32_t id = idesc_f16(BM, I.ncols);
-#pragma unroll
-        for (int mat = 0; mat < 2; ++mat) {
-#pragma unroll
-            for (int k16 = 0; k16 < 2; ++k16) {
-                mma_f16(tmem + sl * 256 + mat * 128, sdesc(fa + mat * (BM * 64) + k16 * 256, 128, 512),
-                        sdesc(fbB + k16 * 256, 128, 512), id, (uint32_t)k16);
-            }
-        }
-        mma_commit(bar(B_TM_FULL + sl));
-        mma_issued = idx + 1;
-        return true;
-    };
-
-    // ---- worker duty (all threads)
-    const int wt = threadIdx.x;     // 0..255
-    const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int h = warp >> 2;        // column half
-    const int m = q * 32 + lane;    // weight row (TMEM lane) of this thread
-    // accumulators: 4 chunks x 16 columns for each matrix, as 8 packed pairs
-    uint64_t accA[4][8], accB[4][8];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
-
-    auto convert = [&](int idx) -> bool {
-        const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
-        // warp-uniform decision: the warp synchronizes below before arriving
-        if (!__all_sync(0xffffffffu, waitp(bar(B_RAW_FULL + sl), (gs / RS) & 1))) return false;
-        const Item I = item(idx / nb);  // read after the barrier that orders it
-        const uint8_t* st = smem + sl * L::STAGE;
-        uint8_t* fa = smem + L::O_F16 + (idx % NF) * F16_SLOT;
-        uint8_t* fbB = fa + F16_A;
-        float* sc = (float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
-        // weights: 256 rows x 32 values of block blk
-        if (WT == MOE_W_Q8_0) {
-#pragma unroll
-            for (int rep = 0; rep < 2; ++rep) {
-                // lanes 0-7 take 8 consecutive rows, lanes 8-15 their second
-                // halves, lanes 16-31 the next 8 rows: every 8-lane phase of the
-                // 16-byte loads and stores touches 8 distinct bank groups
-                const int R = rep * 128 + (wt >> 5) * 16 + (lane & 7) + 8 * (lane >> 4);
-                const int hh = (lane >> 3) & 1;
-                const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
-                const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
-                uint4 o0, o1;
-                cvt_i8x4(v.x, o0.x, o0.y);
-                cvt_i8x4(v.y, o0.z, o0.w);
-                cvt_i8x4(v.z, o1.x, o1.y);
-                cvt_i8x4(v.w, o1.z, o1.w);
-                uint8_t* dst = fa + (R >> 7) * (BM * 64);
-                *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
-                *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
-            }
-        } else {
-            const int R = wt;
-            const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
-            const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            uint8_t* dst = fa + (R >> 7) * (BM * 64);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t hv[4];
-                cvt_u4x8(w4[c], hv);
-                *(uint4*)(dst + f16_off(R & 127, c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            }
-        }
-        // activations: ncols rows x 32 values, units of 16
-        if (wt < 2 * I.ncols) {
-            const int n = (wt >> 5) * 16 + (lane & 7) + 8 * (lane >> 4);  // as for the weights
-            const int hh = (lane >> 3) & 1;
-            const int ch = (blk * 2 + hh) ^ (n & 7);
-            const uint4 v = *(const uint4*)(st + L::O_X + n * 128 + ch * 16);
-            uint4 o0, o1;
-            if (WT == MOE_W_Q8_0) {
-                cvt_i8x4(v.x, o0.x, o0.y);
-                cvt_i8x4(v.y, o0.z, o0.w);
-                cvt_i8x4(v.z, o1.x, o1.y);
-                cvt_i8x4(v.w, o1.z, o1.w);
-            } else {
-                uint32_t a[4], b[4];
-                cvt_i8x8_interleaved(v.x, v.y, a);
-                cvt_i8x8_interleaved(v.z, v.w, b);
-                o0 = make_uint4(a[0], a[1], a[2], a[3]);
-                o1 = make_uint4(b[0], b[1], b[2], b[3]);
-            }
-            *(uint4*)(fbB + f16_off(n, 2 * hh)) = o0;
-            *(uint4*)(fbB + f16_off(n, 2 * hh + 1)) = o1;
-        }
-        // scales of block blk as fp32: dW[256], mW[256], dX[128], sX[128]
-        {
-            const int R = wt;
-            const int si = GU ? (((R >> 7) * KBS + blk) * BM + (R & 127)) : (blk * 2 * BM + R);
-            sc[R] = __half2float(((const __half*)(st + L::O_WS))[si]);
-            if (WT == MOE_W_Q4_1) sc[2 * BM + R] = __half2float(((const __half*)(st + L::O_WM))[si]);
-            if (R < BN) {
-                const __half2 xs = ((const __half2*)(st + L::O_XS))[R * KBS + blk];
-                sc[4 * BM + R] = __low2float(xs);
-                sc[4 * BM + BN + R] = __high2float(xs);
-            }
-        }
-        // make this thread's fp16 operands visible to the tensor core, then one
-        // arrival per warp (an mbarrier is a single word)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(bar(B_F16_FULL + idx % NF));
-            if (blk == KBS - 1) mbar_arrive(bar(B_RAW_EMPTY + sl));
-        }
-        return true;
-    };
-
-    auto epilogue = [&](int idx) -> bool {
-        const int i = idx / nb, b = idx - i * nb;
-        const int sl = idx % NF;
-        // warp-uniform decision: the TMEM loads below are warp-collective
-        if (!__all_sync(0xffffffffu, waitp(bar(B_TM_FULL + sl), (idx / NF) & 1))) return false;
-        tc_fence_after();
-        const Item I = item(i);
-        const float* sc = (const float*)(smem + L::O_SC + (idx % NSC) * SC_SLOT);
-        const float dA = sc[m], dB = sc[BM + m];
-        const float mA = WT == MOE_W_Q4_1 ? sc[2 * BM + m] : 0.0f;
-        const float mB = WT == MOE_W_Q4_1 ? sc[3 * BM + m] : 0.0f;
-        const uint64_t dA2 = pk2(__float_as_uint(dA), __float_as_uint(dA));
-        const uint64_t dB2 = pk2(__float_as_uint(dB), __float_as_uint(dB));
-        const uint64_t mA2 = pk2(__float_as_uint(mA), __float_as_uint(mA));
-        const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
-        const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
-        const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
-        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + sl * 256;
-        const int nch = min(4, max(0, (I.ncols - h * 64) / 16));  // active 16-column chunks
-        // software pipeline: chunk c+1's TMEM loads (and scales) are in flight
-        // while chunk c is scaled and accumulated
-        uint32_t ra[2][16], rb[2][16];
-        uint64_t dxp[8];
-        if (nch > 0) {
-            tmem_ld16(tbase + h * 64, ra[0]);
-            tmem_ld16(tbase + 128 + h * 64, rb[0]);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) dxp[j] = dX2[h * 32 + j];
-            tmem_wait32(ra[0], rb[0]);
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            if (c < nch) {
-                const int cur = c & 1, nxt = cur ^ 1;
-                const int col0 = h * 64 + c * 16;
-                if (c + 1 < nch) {
-                    tmem_ld16(tbase + col0 + 16, ra[nxt]);
-                    tmem_ld16(tbase + 128 + col0 + 16, rb[nxt]);
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint64_t pa = pk2(ra[cur][2 * j], ra[cur][2 * j + 1]);
-                    const uint64_t pb = pk2(rb[cur][2 * j], rb[cur][2 * j + 1]);
-                    accA[c][j] = fma2u(mul2u(dA2, dxp[j]), pa, accA[c][j]);
-                    accB[c][j] = fma2u(mul2u(dB2, dxp[j]), pb, accB[c][j]);
-                    if (WT == MOE_W_Q4_1) {
-                        const uint64_t s2 = sX2[col0 / 2 + j];
-                        accA[c][j] = fma2u(mA2, s2, accA[c][j]);
-                        accB[c][j] = fma2u(mB2, s2, accB[c][j]);
+                if (c < nch) {
+                    const int cur = c & 1, nxt = cur ^ 1;
+                    const int col0 = h * 64 + c * 16;
+                    if (c + 1 < nch) {
+                        tmem_ld16(tbase + col0 + 16, ra[nxt]);
+                        tmem_ld16(tbase + 128 + col0 + 16, rb[nxt]);
                     }
-                }
-                if (c + 1 < nch) {
-                    // next chunk's scales load while its TMEM loads complete
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) dxp[j] = dX2[(col0 + 16) / 2 + j];
-                    tmem_wait32(ra[nxt], rb[nxt]);
-                }
-            }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_TM_EMPTY + sl));
-        if (b == nb - 1) {
-            // item complete: write this thread's row for every valid token
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float a[2], bb[2];
-                    upk2(accA[c][j], a[0], a[1]);
-                    upk2(accB[c][j], bb[0], bb[1]);
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int n = h * 64 + c * 16 + 2 * j + e;
-                        if (n < I.rows) {
-                            float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
-                            if (GU) {
-                                o[0] = silu_mul(a[e], bb[e]);
-                            } else {
-                                o[0] = a[e];
-                                o[BM] = bb[e];
-                            }
+                    for (int j = 0; j < 8; ++j) {
+                        const uint64_t pa = pk2(ra[cur][2 * j], ra[cur][2 * j + 1]);
+                        const uint64_t pb = pk2(rb[cur][2 * j], rb[cur][2 * j + 1]);
+                        const uint64_t dx = dX2[col0 / 2 + j];
+                        accA[c][j] = fma2u(mul2u(dA2, dx), pa, accA[c][j]);
+                        accB[c][j] = fma2u(mul2u(dB2, dx), pb, accB[c][j]);
+                        if (WT == MOE_W_Q4_1) {
+                            const uint64_t s2 = sX2[col0 / 2 + j];
+                            accA[c][j] = fma2u(mA2, s2, accA[c][j]);
+                            accB[c][j] = fma2u(mB2, s2, accB[c][j]);
                         }
                     }
-                    accA[c][j] = accB[c][j] = 0ull;
+                    if (c + 1 < nch) tmem_wait32(ra[nxt], rb[nxt]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(B_TM_EMPTY + tb));
+                mbar_arrive(bar(B_SC_EMPTY + ss));
+            }
+            if (b == nb - 1) {
+                // item complete: write this thread's row for every valid token
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float a[2], bb[2];
+                        upk2(accA[c][j], a[0], a[1]);
+                        upk2(accB[c][j], bb[0], bb[1]);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int n = h * 64 + c * 16 + 2 * j + e;
+                            if (n < I.rows) {
+                                float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
+                                if (GU) {
+                                    o[0] = silu_mul(a[e], bb[e]);
+                                } else {
+                                    o[0] = a[e];
+                                    o[BM] = bb[e];
+                                }
+                            }
+                        }
+                        accA[c][j] = accB[c][j] = 0ull;
+                    }
                 }
             }
         }
-        return true;
-    };
-
-    // Every lane runs every step, and each step's continue/stop decision is
-    // warp-uniform (__all_sync), so the warp-collective TMEM loads never see a
-    // diverged warp; a failed MMA issue only raises the abort flag, which the
-    // next waits observe.
-    bool ok = true;
-    if (is_producer) produce();
-    for (int idx = 0; idx < LOOKAHEAD && idx < total && ok; ++idx)
-        ok = convert(idx);
-    if (ok && is_mma) issue_mma(0);
-    for (int idx = 0; idx < total && ok; ++idx) {
-        if (is_producer) produce();
-        if (is_mma && idx + 1 < total) issue_mma(idx + 1);
-        ok = epilogue(idx);
-        if (ok && idx + LOOKAHEAD < total) ok = convert(idx + LOOKAHEAD);
-    }
-
-    // drain what this CTA started before it may exit (only waits on the abort path)
-    if (is_producer) {
-        for (int gs = (next_stage > RS ? next_stage - RS : 0); gs < next_stage; ++gs) {
-            long long t0 = clock64();
-            while (!mbar_try_wait(bar(B_RAW_FULL + gs % RS), (gs / RS) & 1) &&
-                   clock64() - t0 < TIMEOUT_CYCLES) {
+    } else if (warp < EPI_WARPS + CVT_WARPS) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CVT_REGS));
+        // ---- converters: block idx's raw tiles -> fp16 operand slot idx % NFS
+        // (the layout the MMA descriptors read) and fp32 scales -> slot idx % NSC
+        const int ct = threadIdx.x - EPI_WARPS * 32;  // 0..127
+        const int cw = ct >> 5;
+        for (int idx = 0; idx < total; ++idx) {
+            const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
+            const int fs = idx % NFS, ss = idx % NSC;
+            if (blk == 0 && !wait_warp(bar(B_RAW_FULL + sl), (gs / RS) & 1)) break;
+            if (idx >= NFS && !wait_warp(bar(B_F16_EMPTY + fs), ((idx / NFS) - 1) & 1)) break;
+            if (idx >= NSC && !wait_warp(bar(B_SC_EMPTY + ss), ((idx / NSC) - 1) & 1)) break;
+            const Item I = item(idx / nb);  // read after the barrier that orders it
+            const uint8_t* st = smem + sl * L::STAGE;
+            uint8_t* fa = smem + L::O_F16 + fs * F16_SLOT;
+            uint8_t* fbB = fa + F16_A;
+            float* sc = (float*)(smem + L::O_SC + ss * SC_SLOT);
+            // weights: 256 rows x 32 values of block blk
+            if (WT == MOE_W_Q8_0) {
+#pragma unroll 1
+                for (int rep = 0; rep < 4; ++rep) {
+                    // lanes 0-7 take 8 consecutive rows, lanes 8-15 their second
+                    // halves, lanes 16-31 the next 8 rows: every 8-lane phase of
+                    // the 16-byte loads and stores touches 8 distinct bank groups
+                    const int R = rep * 64 + cw * 16 + (lane & 7) + 8 * (lane >> 4);
+                    const int hh = (lane >> 3) & 1;
+                    const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
+                    const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
+                    uint4 o0, o1;
+                    cvt_i8x4(v.x, o0.x, o0.y);
+                    cvt_i8x4(v.y, o0.z, o0.w);
+                    cvt_i8x4(v.z, o1.x, o1.y);
+                    cvt_i8x4(v.w, o1.z, o1.w);
+                    uint8_t* dst = fa + (R >> 7) * (BM * 64);
+                    *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
+                    *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
+                }
+            } else {
+#pragma unroll 1
+                for (int rep = 0; rep < 2; ++rep) {
+                    const int R = rep * 128 + ct;
+                    const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
+                    const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    uint8_t* dst = fa + (R >> 7) * (BM * 64);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t hv[4];
+                        cvt_u4x8(w4[c], hv);
+                        *(uint4*)(dst + f16_off(R & 127, c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    }
+                }
+            }
+            // activations: ncols rows x 32 values, units of 16 bytes
+#pragma unroll 1
+            for (int rep = 0; rep < 2; ++rep) {
+                const int u = rep * 128 + ct;
+                if (u < 2 * I.ncols) {
+                    const int n = (u >> 5) * 16 + (lane & 7) + 8 * (lane >> 4);  // as for the weights
+                    const int hh = (lane >> 3) & 1;
+                    const int ch = (blk * 2 + hh) ^ (n & 7);
+                    const uint4 v = *(const uint4*)(st + L::O_X + n * 128 + ch * 16);
+                    uint4 o0, o1;
+                    if (WT == MOE_W_Q8_0) {
+                        cvt_i8x4(v.x, o0.x, o0.y);
+                        cvt_i8x4(v.y, o0.z, o0.w);
+                        cvt_i8x4(v.z, o1.x, o1.y);
+                        cvt_i8x4(v.w, o1.z, o1.w);
+                    } else {
+                        uint32_t a[4], b[4];
+                        cvt_i8x8_interleaved(v.x, v.y, a);
+                        cvt_i8x8_interleaved(v.z, v.w, b);
+                        o0 = make_uint4(a[0], a[1], a[2], a[3]);
+                        o1 = make_uint4(b[0], b[1], b[2], b[3]);
+                    }
+                    *(uint4*)(fbB + f16_off(n, 2 * hh)) = o0;
+                    *(uint4*)(fbB + f16_off(n, 2 * hh + 1)) = o1;
+                }
+            }
+            // scales of block blk as fp32: dW[256], mW[256], dX[128], sX[128]
+#pragma unroll 1
+            for (int rep = 0; rep < 2; ++rep) {
+                const int R = rep * 128 + ct;
+                const int si = GU ? (((R >> 7) * KBS + blk) * BM + (R & 127)) : (blk * 2 * BM + R);
+                sc[R] = __half2float(((const __half*)(st + L::O_WS))[si]);
+                if (WT == MOE_W_Q4_1) sc[2 * BM + R] = __half2float(((const __half*)(st + L::O_WM))[si]);
+            }
+            {
+                const __half2 xs = ((const __half2*)(st + L::O_XS))[ct * KBS + blk];
+                sc[4 * BM + ct] = __low2float(xs);
+                sc[4 * BM + BN + ct] = __high2float(xs);
+            }
+            // make this thread's fp16 operands visible to the tensor core, then one
+            // arrival per warp and barrier
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(B_F16_FULL + fs));
+                mbar_arrive(bar(B_SC_FULL + ss));
+                if (blk == KBS - 1) mbar_arrive(bar(B_RAW_EMPTY + sl));
+            }
+        }
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(AUX_REGS));
+        if (warp == EPI_WARPS + CVT_WARPS && lane == 0) {
+            // ---- TMA producer: raw int8 / 4-bit tiles and fp16 scales, KBS
+            // blocks a stage, RS stages in flight
+            int gs = 0;
+            for (; gs < total_stages; ++gs) {
+                const int sl = gs % RS, u = gs / RS;
+                if (u > 0 && !mbar_wait(bar(B_RAW_EMPTY + sl), (u - 1) & 1, abort_flag)) break;
+                const int i = gs / spi, s = gs - i * spi;
+                if (s == 0) {
+                    const Item J = load_item<GU>(P, (int)blockIdx.x + i * (int)gridDim.x);
+                    ring[i % ITEM_RING] = make_int4(J.p, J.r0, J.rows, J.w0);
+                }
+                const Item I = item(i);
+                const uint32_t st = sbase + sl * L::STAGE;
+                const uint32_t fb = bar(B_RAW_FULL + sl);
+                mbar_expect_tx(fb, L::TX);
+                if (GU) {
+                    tma_4d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, 0, I.p);
+                    tma_4d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, 0, I.p);
+                    if (WT == MOE_W_Q4_1) tma_4d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, 0, I.p);
+                } else {
+                    tma_3d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, I.p);
+                    tma_3d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, I.p);
+                    if (WT == MOE_W_Q4_1) tma_3d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, I.p);
+                }
+                tma_2d(&mX, fb, st + L::O_X, s * 128, I.r0);
+                tma_2d(&mXs, fb, st + L::O_XS, s * KBS, I.r0);
+            }
+            // drain the copies still in flight before the CTA may exit (waits
+            // only on the abort path)
+            for (int g = (gs > RS ? gs - RS : 0); g < gs; ++g) {
+                long long t0 = clock64();
+                while (!mbar_try_wait(bar(B_RAW_FULL + g % RS), (g / RS) & 1) &&
+                       clock64() - t0 < TIMEOUT_CYCLES) {
+                }
+            }
+        } else if (warp == EPI_WARPS + CVT_WARPS + 1 && lane == 0) {
+            // ---- MMA issuer: block idx's products into TMEM buffer idx % NTB,
+            // 2 x (M=128, N<=128, K=16) per matrix; one commit releases the
+            // partials to the epilogue, a second the fp16 slot to the converters
+            int idx = 0;
+            for (; idx < total; ++idx) {
+                const int fs = idx % NFS, tb = idx % NTB;
+                if (!mbar_wait(bar(B_F16_FULL + fs), (idx / NFS) & 1, abort_flag)) break;
+                if (idx >= NTB && !mbar_wait(bar(B_TM_EMPTY + tb), ((idx / NTB) - 1) & 1, abort_flag))
+                    break;
+                tc_fence_after();
+                const Item I = item(idx / nb);  // read after the barrier that orders it
+                const uint32_t fa = sbase + L::O_F16 + fs * F16_SLOT;
+                const uint32_t fbB = fa + F16_A;
+                const uint32_t id = idesc_f16(BM, I.ncols);
+#pragma unroll
+                for (int mat = 0; mat < 2; ++mat) {
+#pragma unroll
+                    for (int k16 = 0; k16 < 2; ++k16) {
+                        mma_f16(tmem + tb * 256 + mat * 128,
+                                sdesc(fa + mat * (BM * 64) + k16 * 256, 128, 512),
+                                sdesc(fbB + k16 * 256, 128, 512), id, (uint32_t)k16);
+                    }
+                }
+                mma_commit(bar(B_TM_FULL + tb));
+                mma_commit(bar(B_F16_EMPTY + fs));
+            }
+            // the last committed group must land before TMEM is freed
+            if (idx > 0) {
+                const int last = idx - 1;
+                long long t0 = clock64();
+                while (!mbar_try_wait(bar(B_TM_FULL + last % NTB), (last / NTB) & 1) &&
+                       clock64() - t0 < TIMEOUT_CYCLES) {
+                }
             }
         }
     }
-    if (is_mma && mma_issued > 0) {
-        const int last = mma_issued - 1;
-        long long t0 = clock64();
-        while (!mbar_try_wait(bar(B_TM_FULL + last % NF), (last / NF) & 1) &&
-               clock64() - t0 < TIMEOUT_CYCLES) {
-        }
-    }
+
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) set_error(P.err, MOE_DEV_ERR_TIMEOUT);
     if (warp == 0) {
@@ -762,6 +797,38 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
         std::fprintf(stderr, "\n");
     }
     return r == CUDA_SUCCESS;
+}
+
+// The register split relies on the launch giving every thread exactly
+// LAUNCH_REGS registers (setmaxnreg.inc waits until warpgroup 2 has released
+// enough): check the compiled kernel once, with the shared-memory opt-in,
+// before any launch.
+template <int WT, bool GU>
+bool kernel_ready() {
+    static bool ok = false;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaFuncAttributes a;
+        cudaError_t e = cudaFuncGetAttributes(&a, mmq_tc_kernel<WT, GU>);
+        if (e != cudaSuccess) {
+            if (debug()) std::fprintf(stderr, "moe_q8: mmq_tc attributes: %s\n", cudaGetErrorString(e));
+            return;
+        }
+        if (a.numRegs != LAUNCH_REGS || a.maxThreadsPerBlock < THREADS) {
+            if (debug())
+                std::fprintf(stderr, "moe_q8: mmq_tc built with %d registers / %d threads, want %d / %d\n",
+                             a.numRegs, a.maxThreadsPerBlock, LAUNCH_REGS, THREADS);
+            return;
+        }
+        e = cudaFuncSetAttribute(mmq_tc_kernel<WT, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Lay<WT>::SMEM);
+        if (e != cudaSuccess) {
+            if (debug()) std::fprintf(stderr, "moe_q8: smem attribute failed: %s\n", cudaGetErrorString(e));
+            return;
+        }
+        ok = true;
+    });
+    return ok;
 }
 
 template <int WT, bool GU>
@@ -821,16 +888,13 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     }
     if (!ok) return MOE_ERR_CUDA;
 
+    if (!kernel_ready<WT, GU>()) return MOE_ERR_UNSUPPORTED;
     static int sms = 0;
-    static std::once_flag attr_once;
-    std::call_once(attr_once, [] {
+    static std::once_flag sms_once;
+    std::call_once(sms_once, [] {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel<WT, GU>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
-        if (e != cudaSuccess && debug())
-            std::fprintf(stderr, "moe_q8: smem attribute failed: %s\n", cudaGetErrorString(e));
     });
     Params P;
     P.tiles = (const int4*)(ws + W.tiles);
@@ -856,8 +920,10 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
 bool mmq_tc_supported(int wtype, bool gateup, int d, int f) {
     if (wtype != MOE_W_Q8_0 && wtype != MOE_W_Q4_1) return false;
     if (d % 256 || f % 128) return false;  // whole 128-row weight tiles, 128-wide K stages
-    (void)gateup;
-    return tc::encode_fn() != nullptr;
+    if (tc::encode_fn() == nullptr) return false;
+    if (wtype == MOE_W_Q8_0)
+        return gateup ? tc::kernel_ready<MOE_W_Q8_0, true>() : tc::kernel_ready<MOE_W_Q8_0, false>();
+    return gateup ? tc::kernel_ready<MOE_W_Q4_1, true>() : tc::kernel_ready<MOE_W_Q4_1, false>();
 }
 
 int launch_mmq_tc(int wtype, bool gateup, const uint8_t* group_base, size_t slot_stride,
