@@ -162,12 +162,32 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete; false on abort or timeout.
+// Wait for the phase of `parity` to complete; false on abort or timeout.  The
+// thread may sleep in hardware until the phase completes.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > TIMEOUT_CYCLES) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Two phases (the second only if need2), both probed before either wait.
+__device__ __forceinline__ bool mbar_wait2(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2,
+                                           bool need2, volatile int* abort_flag) {
+    bool d1 = mbar_test_wait(b1, p1);
+    bool d2 = !need2 || mbar_test_wait(b2, p2);
+    if (d1 && d2) return true;
+    long long t0 = clock64();
+    while (true) {
+        if (!d1) d1 = mbar_try_wait_sleep(b1, p1);
+        if (d1 && !d2) d2 = mbar_try_wait_sleep(b2, p2);
+        if (d1 && d2) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > TIMEOUT_CYCLES) {
             *abort_flag = 1;
@@ -466,6 +486,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         return __all_sync(0xffffffffu, done);
     };
 
+    // As wait_warp for two phases at once: both probes are issued back to back
+    // (a probe of a completed phase still costs a shared-memory round trip)
+    // and one vote makes the result warp-uniform.
+    auto wait_warp2 = [&](uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2) -> bool {
+        bool d1 = mbar_test_wait(b1, p1);
+        bool d2 = mbar_test_wait(b2, p2);
+        if (!(d1 && d2)) {
+            long long t0 = clock64();
+            while (true) {
+                if (!d1) d1 = mbar_try_wait_sleep(b1, p1);
+                if (d1 && !d2) d2 = mbar_try_wait_sleep(b2, p2);
+                if (d1 && d2) break;
+                if (*abort_flag) break;
+                if (clock64() - t0 > TIMEOUT_CYCLES) {
+                    *abort_flag = 1;
+                    break;
+                }
+            }
+        }
+        return __all_sync(0xffffffffu, d1 && d2);
+    };
+
     if (warp < EPI_WARPS) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
         // ---- epilogue: for block idx, warp w reads TMEM lane quarter w % 4 (its
@@ -480,14 +522,31 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
-        for (int idx = 0; idx < total; ++idx) {
-            const int i = idx / nb, b = idx - i * nb;
-            const int tb = idx % NTB, ss = idx % NSC;
-            // warp-uniform decisions: the TMEM loads below are warp-collective
-            if (!wait_warp(bar(B_TM_FULL + tb), (idx / NTB) & 1)) break;
-            if (!wait_warp(bar(B_SC_FULL + ss), (idx / NSC) & 1)) break;
+        auto chunks = [&](const Item& I) { return min(4, max(0, (I.ncols - h * 64) / 16)); };
+        const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
+        // The TMEM partials stream through two register buffers in 16-column
+        // chunks: the load of the next chunk -- across block boundaries too --
+        // is in flight while the current one is scaled and accumulated.  Block
+        // idx occupies chunk positions 0-3 (buffers 0, 1, 0, 1); the next
+        // block's first chunk is loaded at position 3 into buffer 0.
+        uint32_t ra[2][16], rb[2][16];
+        int i = 0, b = 0;  // item and block within the item of idx
+        bool ok = total > 0 && wait_warp2(bar(B_TM_FULL), 0, bar(B_SC_FULL), 0);
+        Item I, In;
+        int nch = 0, nch_n = 0;
+        if (ok) {
             tc_fence_after();
-            const Item I = item(i);
+            I = item(0);
+            nch = chunks(I);
+            if (nch > 0) {
+                tmem_ld16(lanes + h * 64, ra[0]);
+                tmem_ld16(lanes + 128 + h * 64, rb[0]);
+            }
+            tmem_wait32(ra[0], rb[0]);
+        }
+        for (int idx = 0; ok && idx < total; ++idx) {
+            const int tb = idx % NTB, ss = idx % NSC;
+            const uint32_t tbase = lanes + tb * 256;
             const float* sc = (const float*)(smem + L::O_SC + ss * SC_SLOT);
             const float dA = sc[m], dB = sc[BM + m];
             const float mA = WT == MOE_W_Q4_1 ? sc[2 * BM + m] : 0.0f;
@@ -498,25 +557,38 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
             const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
             const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + tb * 256;
-            const int nch = min(4, max(0, (I.ncols - h * 64) / 16));  // active 16-column chunks
-            // software pipeline: chunk c+1's TMEM loads (and scales) are in flight
-            // while chunk c is scaled and accumulated
-            uint32_t ra[2][16], rb[2][16];
-            if (nch > 0) {
-                tmem_ld16(tbase + h * 64, ra[0]);
-                tmem_ld16(tbase + 128 + h * 64, rb[0]);
-                tmem_wait32(ra[0], rb[0]);
-            }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                if (c < nch) {
-                    const int cur = c & 1, nxt = cur ^ 1;
-                    const int col0 = h * 64 + c * 16;
+                const int cur = c & 1, nxt = cur ^ 1;
+                const int col0 = h * 64 + c * 16;
+                if (c < 3) {
                     if (c + 1 < nch) {
                         tmem_ld16(tbase + col0 + 16, ra[nxt]);
                         tmem_ld16(tbase + 128 + col0 + 16, rb[nxt]);
                     }
+                } else {
+                    // every partial of block idx is in registers: free its buffer
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_TM_EMPTY + tb));
+                    const int n1 = idx + 1;
+                    if (n1 < total) {
+                        // warp-uniform decision: the TMEM loads below are warp-collective
+                        ok = wait_warp2(bar(B_TM_FULL + n1 % NTB), (n1 / NTB) & 1,
+                                        bar(B_SC_FULL + n1 % NSC), (n1 / NSC) & 1);
+                        if (ok) {
+                            tc_fence_after();
+                            In = item(b + 1 == nb ? i + 1 : i);
+                            nch_n = chunks(In);
+                            if (nch_n > 0) {
+                                const uint32_t nbase = lanes + (n1 % NTB) * 256 + h * 64;
+                                tmem_ld16(nbase, ra[0]);
+                                tmem_ld16(nbase + 128, rb[0]);
+                            }
+                        }
+                    }
+                }
+                if (c < nch) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const uint64_t pa = pk2(ra[cur][2 * j], ra[cur][2 * j + 1]);
@@ -530,15 +602,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                             accB[c][j] = fma2u(mB2, s2, accB[c][j]);
                         }
                     }
-                    if (c + 1 < nch) tmem_wait32(ra[nxt], rb[nxt]);
                 }
+                tmem_wait32(ra[nxt], rb[nxt]);  // the loads issued at this position
             }
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(B_TM_EMPTY + tb));
-                mbar_arrive(bar(B_SC_EMPTY + ss));
-            }
+            if (lane == 0) mbar_arrive(bar(B_SC_EMPTY + ss));
             if (b == nb - 1) {
                 // item complete: write this thread's row for every valid token
 #pragma unroll
@@ -564,21 +632,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                         accA[c][j] = accB[c][j] = 0ull;
                     }
                 }
+                b = 0;
+                ++i;
+            } else {
+                ++b;
             }
+            I = In;
+            nch = nch_n;
         }
+        // no TMEM load may be outstanding when the CTA frees TMEM
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
     } else if (warp < EPI_WARPS + CVT_WARPS) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CVT_REGS));
         // ---- converters: block idx's raw tiles -> fp16 operand slot idx % NFS
         // (the layout the MMA descriptors read) and fp32 scales -> slot idx % NSC
         const int ct = threadIdx.x - EPI_WARPS * 32;  // 0..127
+        int ci = 0, cb = 0;                            // item and block within the item of idx
         const int cw = ct >> 5;
         for (int idx = 0; idx < total; ++idx) {
             const int gs = idx / KBS, sl = gs % RS, blk = idx % KBS;
             const int fs = idx % NFS, ss = idx % NSC;
+            static_assert(NSC >= NFS, "slot reuse order");
+            if (idx >= NSC) {
+                if (!wait_warp2(bar(B_F16_EMPTY + fs), ((idx / NFS) - 1) & 1, bar(B_SC_EMPTY + ss),
+                                ((idx / NSC) - 1) & 1))
+                    break;
+            } else if (idx >= NFS && !wait_warp(bar(B_F16_EMPTY + fs), ((idx / NFS) - 1) & 1)) {
+                break;
+            }
             if (blk == 0 && !wait_warp(bar(B_RAW_FULL + sl), (gs / RS) & 1)) break;
-            if (idx >= NFS && !wait_warp(bar(B_F16_EMPTY + fs), ((idx / NFS) - 1) & 1)) break;
-            if (idx >= NSC && !wait_warp(bar(B_SC_EMPTY + ss), ((idx / NSC) - 1) & 1)) break;
-            const Item I = item(idx / nb);  // read after the barrier that orders it
+            const Item I = item(ci);  // read after the barrier that orders it
+            if (++cb == nb) {
+                cb = 0;
+                ++ci;
+            }
             const uint8_t* st = smem + sl * L::STAGE;
             uint8_t* fa = smem + L::O_F16 + fs * F16_SLOT;
             uint8_t* fbB = fa + F16_A;
@@ -711,13 +798,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             // 2 x (M=128, N<=128, K=16) per matrix; one commit releases the
             // partials to the epilogue, a second the fp16 slot to the converters
             int idx = 0;
+            int mi = 0, mb = 0;  // item and block within the item of idx
             for (; idx < total; ++idx) {
                 const int fs = idx % NFS, tb = idx % NTB;
-                if (!mbar_wait(bar(B_F16_FULL + fs), (idx / NFS) & 1, abort_flag)) break;
-                if (idx >= NTB && !mbar_wait(bar(B_TM_EMPTY + tb), ((idx / NTB) - 1) & 1, abort_flag))
+                if (!mbar_wait2(bar(B_F16_FULL + fs), (idx / NFS) & 1, bar(B_TM_EMPTY + tb),
+                                ((idx / NTB) - 1) & 1, idx >= NTB, abort_flag))
                     break;
                 tc_fence_after();
-                const Item I = item(idx / nb);  // read after the barrier that orders it
+                const Item I = item(mi);  // read after the barrier that orders it
+                if (++mb == nb) {
+                    mb = 0;
+                    ++mi;
+                }
                 const uint32_t fa = sbase + L::O_F16 + fs * F16_SLOT;
                 const uint32_t fbB = fa + F16_A;
                 const uint32_t id = idesc_f16(BM, I.ncols);
