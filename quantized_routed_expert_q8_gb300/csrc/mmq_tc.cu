@@ -261,29 +261,32 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 16 consecutive TMEM columns of this thread's lane; the values are valid only
-// after tmem_wait16 on the same registers.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+// Four 16-column TMEM loads (columns ta, ta + 16 of one matrix and tb, tb + 16
+// of the other) and the wait for them in one statement, so the registers are
+// defined only once the data has landed.
+__device__ __forceinline__ void tmem_ld16x4_wait(uint32_t ta, uint32_t tb, uint32_t (&r)[4][16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-        "%12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
-// Wait for this thread's outstanding TMEM loads.  The loaded registers pass
-// through the statement so no use of them can be scheduled before the wait.
-__device__ __forceinline__ void tmem_wait32(uint32_t (&a)[16], uint32_t (&b)[16]) {
-    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, "
+        "%8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, "
+        "%24, %25, %26, %27, %28, %29, %30, %31}, [%65];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32, %33, %34, %35, %36, %37, %38, %39, "
+        "%40, %41, %42, %43, %44, %45, %46, %47}, [%66];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48, %49, %50, %51, %52, %53, %54, %55, "
+        "%56, %57, %58, %59, %60, %61, %62, %63}, [%67];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
-        : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
-          "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]),
-          "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]),
-          "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]),
-          "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
-        :
+        : "=r"(r[0][0]), "=r"(r[0][1]), "=r"(r[0][2]), "=r"(r[0][3]), "=r"(r[0][4]), "=r"(r[0][5]),
+          "=r"(r[0][6]), "=r"(r[0][7]), "=r"(r[0][8]), "=r"(r[0][9]), "=r"(r[0][10]), "=r"(r[0][11]),
+          "=r"(r[0][12]), "=r"(r[0][13]), "=r"(r[0][14]), "=r"(r[0][15]), "=r"(r[1][0]), "=r"(r[1][1]),
+          "=r"(r[1][2]), "=r"(r[1][3]), "=r"(r[1][4]), "=r"(r[1][5]), "=r"(r[1][6]), "=r"(r[1][7]),
+          "=r"(r[1][8]), "=r"(r[1][9]), "=r"(r[1][10]), "=r"(r[1][11]), "=r"(r[1][12]), "=r"(r[1][13]),
+          "=r"(r[1][14]), "=r"(r[1][15]), "=r"(r[2][0]), "=r"(r[2][1]), "=r"(r[2][2]), "=r"(r[2][3]),
+          "=r"(r[2][4]), "=r"(r[2][5]), "=r"(r[2][6]), "=r"(r[2][7]), "=r"(r[2][8]), "=r"(r[2][9]),
+          "=r"(r[2][10]), "=r"(r[2][11]), "=r"(r[2][12]), "=r"(r[2][13]), "=r"(r[2][14]), "=r"(r[2][15]),
+          "=r"(r[3][0]), "=r"(r[3][1]), "=r"(r[3][2]), "=r"(r[3][3]), "=r"(r[3][4]), "=r"(r[3][5]),
+          "=r"(r[3][6]), "=r"(r[3][7]), "=r"(r[3][8]), "=r"(r[3][9]), "=r"(r[3][10]), "=r"(r[3][11]),
+          "=r"(r[3][12]), "=r"(r[3][13]), "=r"(r[3][14]), "=r"(r[3][15])
+        : "r"(ta), "r"(ta + 16), "r"(tb), "r"(tb + 16)
         : "memory");
 }
 
@@ -522,31 +525,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
-        auto chunks = [&](const Item& I) { return min(4, max(0, (I.ncols - h * 64) / 16)); };
         const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
-        // The TMEM partials stream through two register buffers in 16-column
-        // chunks: the load of the next chunk -- across block boundaries too --
-        // is in flight while the current one is scaled and accumulated.  Block
-        // idx occupies chunk positions 0-3 (buffers 0, 1, 0, 1); the next
-        // block's first chunk is loaded at position 3 into buffer 0.
-        uint32_t ra[2][16], rb[2][16];
         int i = 0, b = 0;  // item and block within the item of idx
-        bool ok = total > 0 && wait_warp2(bar(B_TM_FULL), 0, bar(B_SC_FULL), 0);
-        Item I, In;
-        int nch = 0, nch_n = 0;
-        if (ok) {
-            tc_fence_after();
-            I = item(0);
-            nch = chunks(I);
-            if (nch > 0) {
-                tmem_ld16(lanes + h * 64, ra[0]);
-                tmem_ld16(lanes + 128 + h * 64, rb[0]);
-            }
-            tmem_wait32(ra[0], rb[0]);
-        }
-        for (int idx = 0; ok && idx < total; ++idx) {
+        for (int idx = 0; idx < total; ++idx) {
             const int tb = idx % NTB, ss = idx % NSC;
-            const uint32_t tbase = lanes + tb * 256;
+            // warp-uniform decision: the TMEM loads below are warp-collective
+            if (!wait_warp2(bar(B_TM_FULL + tb), (idx / NTB) & 1, bar(B_SC_FULL + ss), (idx / NSC) & 1))
+                break;
+            tc_fence_after();
+            const Item I = item(i);
+            const int nch = min(4, max(0, (I.ncols - h * 64) / 16));  // active 16-column chunks
+            const uint32_t tbase = lanes + tb * 256 + h * 64;
             const float* sc = (const float*)(smem + L::O_SC + ss * SC_SLOT);
             const float dA = sc[m], dB = sc[BM + m];
             const float mA = WT == MOE_W_Q4_1 ? sc[2 * BM + m] : 0.0f;
@@ -555,58 +544,40 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t dB2 = pk2(__float_as_uint(dB), __float_as_uint(dB));
             const uint64_t mA2 = pk2(__float_as_uint(mA), __float_as_uint(mA));
             const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
-            const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM);       // pairs
-            const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN);  // pairs
+            const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + h * 64);
+            const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN + h * 64);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int cur = c & 1, nxt = cur ^ 1;
-                const int col0 = h * 64 + c * 16;
-                if (c < 3) {
-                    if (c + 1 < nch) {
-                        tmem_ld16(tbase + col0 + 16, ra[nxt]);
-                        tmem_ld16(tbase + 128 + col0 + 16, rb[nxt]);
-                    }
-                } else {
-                    // every partial of block idx is in registers: free its buffer
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_TM_EMPTY + tb));
-                    const int n1 = idx + 1;
-                    if (n1 < total) {
-                        // warp-uniform decision: the TMEM loads below are warp-collective
-                        ok = wait_warp2(bar(B_TM_FULL + n1 % NTB), (n1 / NTB) & 1,
-                                        bar(B_SC_FULL + n1 % NSC), (n1 / NSC) & 1);
-                        if (ok) {
-                            tc_fence_after();
-                            In = item(b + 1 == nb ? i + 1 : i);
-                            nch_n = chunks(In);
-                            if (nch_n > 0) {
-                                const uint32_t nbase = lanes + (n1 % NTB) * 256 + h * 64;
-                                tmem_ld16(nbase, ra[0]);
-                                tmem_ld16(nbase + 128, rb[0]);
-                            }
-                        }
-                    }
-                }
-                if (c < nch) {
+            for (int c2 = 0; c2 < 4; c2 += 2) {
+                if (c2 >= nch) continue;
+                // chunks c2 and c2 + 1 of both matrices in one round trip
+                uint32_t r[4][16];
+                tmem_ld16x4_wait(tbase + c2 * 16, tbase + 128 + c2 * 16, r);
+#pragma unroll
+                for (int c = c2; c < c2 + 2; ++c) {
+                    if (c >= nch) continue;
+                    const uint32_t(&ra)[16] = r[c - c2];
+                    const uint32_t(&rb)[16] = r[2 + c - c2];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const uint64_t pa = pk2(ra[cur][2 * j], ra[cur][2 * j + 1]);
-                        const uint64_t pb = pk2(rb[cur][2 * j], rb[cur][2 * j + 1]);
-                        const uint64_t dx = dX2[col0 / 2 + j];
+                        const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
+                        const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
+                        const uint64_t dx = dX2[c * 8 + j];
                         accA[c][j] = fma2u(mul2u(dA2, dx), pa, accA[c][j]);
                         accB[c][j] = fma2u(mul2u(dB2, dx), pb, accB[c][j]);
                         if (WT == MOE_W_Q4_1) {
-                            const uint64_t s2 = sX2[col0 / 2 + j];
+                            const uint64_t s2 = sX2[c * 8 + j];
                             accA[c][j] = fma2u(mA2, s2, accA[c][j]);
                             accB[c][j] = fma2u(mB2, s2, accB[c][j]);
                         }
                     }
                 }
-                tmem_wait32(ra[nxt], rb[nxt]);  // the loads issued at this position
             }
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_SC_EMPTY + ss));
+            if (lane == 0) {
+                mbar_arrive(bar(B_TM_EMPTY + tb));
+                mbar_arrive(bar(B_SC_EMPTY + ss));
+            }
             if (b == nb - 1) {
                 // item complete: write this thread's row for every valid token
 #pragma unroll
@@ -637,8 +608,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
                 ++b;
             }
-            I = In;
-            nch = nch_n;
         }
         // no TMEM load may be outstanding when the CTA frees TMEM
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
