@@ -639,33 +639,58 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint8_t* fa = smem + L::O_F16 + fs * F16_SLOT;
             uint8_t* fbB = fa + F16_A;
             float* sc = (float*)(smem + L::O_SC + ss * SC_SLOT);
+            // Thread ct's units: weight rows R0 + 64 * rep (Q8_0: both 16-byte
+            // halves split over lanes; Q4_1: one 16-byte row ct + 128 * rep) and
+            // tokens R0, R0 + 64.  Lanes 0-7 take 8 consecutive rows, lanes 8-15
+            // their second halves, lanes 16-31 the next 8 rows, so every 8-lane
+            // phase of the 16-byte loads and stores touches 8 distinct bank groups.
+            // All shared-memory loads of the block are issued before any conversion.
+            const int R0 = cw * 16 + (lane & 7) + 8 * (lane >> 4);
+            const int hh = (lane >> 3) & 1;
+            const int ch = (blk * 2 + hh) ^ (R0 & 7);  // 128-byte TMA swizzle (R0 + 64 * k alike)
+            constexpr int NW = WT == MOE_W_Q8_0 ? 4 : 2;
+            uint4 wv[NW];
+#pragma unroll
+            for (int rep = 0; rep < NW; ++rep) {
+                if (WT == MOE_W_Q8_0) {
+                    wv[rep] = *(const uint4*)(st + L::O_W + (rep * 64 + R0) * 128 + ch * 16);
+                } else {
+                    const int R = rep * 128 + ct;
+                    wv[rep] = *(const uint4*)(st + L::O_W + R * 64 + ((blk ^ ((R >> 1) & 3)) * 16));
+                }
+            }
+            const bool x0 = cw * 16 < I.ncols, x1 = cw * 16 + 64 < I.ncols;  // tokens R0, R0 + 64
+            uint4 xv[2];
+            xv[0] = x0 ? *(const uint4*)(st + L::O_X + R0 * 128 + ch * 16) : make_uint4(0, 0, 0, 0);
+            xv[1] = x1 ? *(const uint4*)(st + L::O_X + (R0 + 64) * 128 + ch * 16) : make_uint4(0, 0, 0, 0);
+            // scales of block blk: dW (and mW) of rows ct, ct + 128; dX, sX of token ct
+            const int si0 = GU ? (blk * BM + ct) : (blk * 2 * BM + ct);
+            const int si1 = GU ? ((KBS + blk) * BM + ct) : (blk * 2 * BM + 128 + ct);
+            const __half* ws = (const __half*)(st + L::O_WS);
+            const __half dw0 = ws[si0], dw1 = ws[si1];
+            __half mw0 = __ushort_as_half(0), mw1 = __ushort_as_half(0);
+            if (WT == MOE_W_Q4_1) {
+                const __half* wm = (const __half*)(st + L::O_WM);
+                mw0 = wm[si0];
+                mw1 = wm[si1];
+            }
+            const __half2 xs = ((const __half2*)(st + L::O_XS))[ct * KBS + blk];
             // weights: 256 rows x 32 values of block blk
-            if (WT == MOE_W_Q8_0) {
-#pragma unroll 1
-                for (int rep = 0; rep < 4; ++rep) {
-                    // lanes 0-7 take 8 consecutive rows, lanes 8-15 their second
-                    // halves, lanes 16-31 the next 8 rows: every 8-lane phase of
-                    // the 16-byte loads and stores touches 8 distinct bank groups
-                    const int R = rep * 64 + cw * 16 + (lane & 7) + 8 * (lane >> 4);
-                    const int hh = (lane >> 3) & 1;
-                    const int ch = (blk * 2 + hh) ^ (R & 7);  // 128-byte TMA swizzle
-                    const uint4 v = *(const uint4*)(st + L::O_W + R * 128 + ch * 16);
+#pragma unroll
+            for (int rep = 0; rep < NW; ++rep) {
+                if (WT == MOE_W_Q8_0) {
+                    const int R = rep * 64 + R0;
                     uint4 o0, o1;
-                    cvt_i8x4(v.x, o0.x, o0.y);
-                    cvt_i8x4(v.y, o0.z, o0.w);
-                    cvt_i8x4(v.z, o1.x, o1.y);
-                    cvt_i8x4(v.w, o1.z, o1.w);
+                    cvt_i8x4(wv[rep].x, o0.x, o0.y);
+                    cvt_i8x4(wv[rep].y, o0.z, o0.w);
+                    cvt_i8x4(wv[rep].z, o1.x, o1.y);
+                    cvt_i8x4(wv[rep].w, o1.z, o1.w);
                     uint8_t* dst = fa + (R >> 7) * (BM * 64);
                     *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
                     *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
-                }
-            } else {
-#pragma unroll 1
-                for (int rep = 0; rep < 2; ++rep) {
+                } else {
                     const int R = rep * 128 + ct;
-                    const int ch = blk ^ ((R >> 1) & 3);  // 64-byte TMA swizzle
-                    const uint4 v = *(const uint4*)(st + L::O_W + R * 64 + ch * 16);
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    const uint32_t w4[4] = {wv[rep].x, wv[rep].y, wv[rep].z, wv[rep].w};
                     uint8_t* dst = fa + (R >> 7) * (BM * 64);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -675,25 +700,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            // activations: ncols rows x 32 values, units of 16 bytes
-#pragma unroll 1
-            for (int rep = 0; rep < 2; ++rep) {
-                const int u = rep * 128 + ct;
-                if (u < 2 * I.ncols) {
-                    const int n = (u >> 5) * 16 + (lane & 7) + 8 * (lane >> 4);  // as for the weights
-                    const int hh = (lane >> 3) & 1;
-                    const int ch = (blk * 2 + hh) ^ (n & 7);
-                    const uint4 v = *(const uint4*)(st + L::O_X + n * 128 + ch * 16);
+            // activations: tokens R0 and R0 + 64 of the MMA's ncols columns
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (k == 0 ? x0 : x1) {
+                    const int n = R0 + 64 * k;
                     uint4 o0, o1;
                     if (WT == MOE_W_Q8_0) {
-                        cvt_i8x4(v.x, o0.x, o0.y);
-                        cvt_i8x4(v.y, o0.z, o0.w);
-                        cvt_i8x4(v.z, o1.x, o1.y);
-                        cvt_i8x4(v.w, o1.z, o1.w);
+                        cvt_i8x4(xv[k].x, o0.x, o0.y);
+                        cvt_i8x4(xv[k].y, o0.z, o0.w);
+                        cvt_i8x4(xv[k].z, o1.x, o1.y);
+                        cvt_i8x4(xv[k].w, o1.z, o1.w);
                     } else {
                         uint32_t a[4], b[4];
-                        cvt_i8x8_interleaved(v.x, v.y, a);
-                        cvt_i8x8_interleaved(v.z, v.w, b);
+                        cvt_i8x8_interleaved(xv[k].x, xv[k].y, a);
+                        cvt_i8x8_interleaved(xv[k].z, xv[k].w, b);
                         o0 = make_uint4(a[0], a[1], a[2], a[3]);
                         o1 = make_uint4(b[0], b[1], b[2], b[3]);
                     }
@@ -701,19 +722,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     *(uint4*)(fbB + f16_off(n, 2 * hh + 1)) = o1;
                 }
             }
-            // scales of block blk as fp32: dW[256], mW[256], dX[128], sX[128]
-#pragma unroll 1
-            for (int rep = 0; rep < 2; ++rep) {
-                const int R = rep * 128 + ct;
-                const int si = GU ? (((R >> 7) * KBS + blk) * BM + (R & 127)) : (blk * 2 * BM + R);
-                sc[R] = __half2float(((const __half*)(st + L::O_WS))[si]);
-                if (WT == MOE_W_Q4_1) sc[2 * BM + R] = __half2float(((const __half*)(st + L::O_WM))[si]);
+            // scales as fp32: dW[256], mW[256], dX[128], sX[128]
+            sc[ct] = __half2float(dw0);
+            sc[128 + ct] = __half2float(dw1);
+            if (WT == MOE_W_Q4_1) {
+                sc[2 * BM + ct] = __half2float(mw0);
+                sc[2 * BM + 128 + ct] = __half2float(mw1);
             }
-            {
-                const __half2 xs = ((const __half2*)(st + L::O_XS))[ct * KBS + blk];
-                sc[4 * BM + ct] = __low2float(xs);
-                sc[4 * BM + BN + ct] = __high2float(xs);
-            }
+            sc[4 * BM + ct] = __low2float(xs);
+            sc[4 * BM + BN + ct] = __high2float(xs);
             // make this thread's fp16 operands visible to the tensor core, then one
             // arrival per warp and barrier
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
