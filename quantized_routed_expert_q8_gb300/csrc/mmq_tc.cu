@@ -544,32 +544,47 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t dB2 = pk2(__float_as_uint(dB), __float_as_uint(dB));
             const uint64_t mA2 = pk2(__float_as_uint(mA), __float_as_uint(mA));
             const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
-            const uint64_t* dX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + h * 64);
-            const uint64_t* sX2 = reinterpret_cast<const uint64_t*>(sc + 4 * BM + BN + h * 64);
+            // token scales as 16-byte loads (two pairs each, the same address in
+            // every lane); a chunk's loads are issued before the work that hides
+            // their latency
+            const ulonglong2* dX4 = reinterpret_cast<const ulonglong2*>(sc + 4 * BM + h * 64);
+            const ulonglong2* sX4 = reinterpret_cast<const ulonglong2*>(sc + 4 * BM + BN + h * 64);
+            auto scale = [&](int c, const uint32_t(&ra)[16], const uint32_t(&rb)[16],
+                             const ulonglong2(&dx)[4], const ulonglong2(&sx)[4]) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
+                    const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
+                    const uint64_t d2 = (j & 1) ? dx[j >> 1].y : dx[j >> 1].x;
+                    accA[c][j] = fma2u(mul2u(dA2, d2), pa, accA[c][j]);
+                    accB[c][j] = fma2u(mul2u(dB2, d2), pb, accB[c][j]);
+                    if (WT == MOE_W_Q4_1) {
+                        const uint64_t s2 = (j & 1) ? sx[j >> 1].y : sx[j >> 1].x;
+                        accA[c][j] = fma2u(mA2, s2, accA[c][j]);
+                        accB[c][j] = fma2u(mB2, s2, accB[c][j]);
+                    }
+                }
+            };
+            auto scales = [&](int c, ulonglong2(&dx)[4], ulonglong2(&sx)[4]) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dx[k] = dX4[c * 4 + k];
+                if (WT == MOE_W_Q4_1) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) sx[k] = sX4[c * 4 + k];
+                }
+            };
 #pragma unroll
             for (int c2 = 0; c2 < 4; c2 += 2) {
                 if (c2 >= nch) continue;
+                ulonglong2 dx[4], sx[4];
+                scales(c2, dx, sx);  // in flight during the TMEM round trip
                 // chunks c2 and c2 + 1 of both matrices in one round trip
                 uint32_t r[4][16];
                 tmem_ld16x4_wait(tbase + c2 * 16, tbase + 128 + c2 * 16, r);
-#pragma unroll
-                for (int c = c2; c < c2 + 2; ++c) {
-                    if (c >= nch) continue;
-                    const uint32_t(&ra)[16] = r[c - c2];
-                    const uint32_t(&rb)[16] = r[2 + c - c2];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
-                        const uint64_t pb = pk2(rb[2 * j], rb[2 * j + 1]);
-                        const uint64_t dx = dX2[c * 8 + j];
-                        accA[c][j] = fma2u(mul2u(dA2, dx), pa, accA[c][j]);
-                        accB[c][j] = fma2u(mul2u(dB2, dx), pb, accB[c][j]);
-                        if (WT == MOE_W_Q4_1) {
-                            const uint64_t s2 = sX2[c * 8 + j];
-                            accA[c][j] = fma2u(mA2, s2, accA[c][j]);
-                            accB[c][j] = fma2u(mB2, s2, accB[c][j]);
-                        }
-                    }
+                scale(c2, r[0], r[2], dx, sx);
+                if (c2 + 1 < nch) {
+                    scales(c2 + 1, dx, sx);
+                    scale(c2 + 1, r[1], r[3], dx, sx);
                 }
             }
             tc_fence_before();
