@@ -168,22 +168,50 @@ def pci_bus_id(dev):
 
 # ------------------------------------------------------------ bytes / ops --
 
+# FP32 operations per block-scale partial in the MMQ epilogue: fma(dW*dX, I, acc)
+# is a multiply and an FMA; Q4_1 adds fma(mW, sX, acc).
+ALU_OPS_PER_PARTIAL = {0: 2, 1: 3}  # by weight type (0 Q8_0, 1 Q4_1)
+FP32_LANES_PER_SM = 128
+MAX_SM_MHZ = 2070.0  # GB300 maximum SM clock
+
+
+def alu_peak_ops(sms: int, mhz: float = MAX_SM_MHZ) -> float:
+    """FP32 operations per second, an FMA counted as one operation: SMs x 128
+    lanes x clock."""
+    return sms * FP32_LANES_PER_SM * mhz * 1e6
+
+
 def layer_accounting(cfg, n_active: int, rec_bytes: int, R: int):
+    """Per stage (bound, amount): algorithmic bytes for the HBM-bound stages; for
+    the MMQ stages the FP32 operations of the block scaling (block-scale partials
+    x operations per partial), the arithmetic their time is bound by (the
+    integer block dots on the tensor cores need less: see mmq_tensor_flops)."""
     T, d, f, K = cfg.T, cfg.d, cfg.f, cfg.K
     q8 = 1.125  # bytes per q8_1 value: int8 plus (d, s) fp16 per 32
+    per = ALU_OPS_PER_PARTIAL[cfg.wtype]
     stages = {
         "slot_map": ("hbm", T * K * 4 * 4),
         "quantize_scatter": ("hbm", T * d * 4 + R * d * q8 + T * K * 4),
         "group_gather": ("hbm", 2 * n_active * rec_bytes),
-        "mmq_gateup": ("tensor", 2.0 * R * 2 * f * d),
+        "mmq_gateup": ("alu", per * R * 2.0 * f * (d // 32)),
         "requant_hidden": ("hbm", R * f * 4 + R * f * q8),
-        "mmq_down": ("tensor", 2.0 * R * d * f),
+        "mmq_down": ("alu", per * R * 1.0 * d * (f // 32)),
         "combine_topk": ("hbm", R * d * 4 + T * d * 4 + T * K * 8),
     }
     total_bytes = (T * d * 4 + 2 * R * d * q8 + 2 * R * f * 4 + 2 * R * f * q8 + 2 * R * d * 4
                    + T * d * 4 + 6 * R * 4 + 3 * n_active * rec_bytes)
     ops = 2.0 * R * 3 * f * d
     return stages, total_bytes, ops
+
+
+def mmq_tensor_flops(cfg, R: int, stage: str) -> float:
+    """Flops of the integer block dots of an MMQ stage (2 per multiply-add)."""
+    return 2.0 * R * (2 * cfg.f * cfg.d if stage == "mmq_gateup" else cfg.d * cfg.f)
+
+
+def alu_partials(cfg, R: int) -> float:
+    """Block-scale partials of the layer: one per output element per 32-block."""
+    return R * 2.0 * cfg.f * (cfg.d // 32) + R * 1.0 * cfg.d * (cfg.f // 32)
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a
@@ -361,11 +389,16 @@ def run_gpu(args, rank, world, local_rank):
     dom_name = stage_names[dom]
     bound, amount = stages[dom_name]
     sec = mean_stage[dom] / 1e3
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = alu_peak_ops(sms)
     if bound == "hbm":
         achieved, peak, unit = amount / sec / 1e9, hbm, "GB/s"
+        peak_note = f"{peak_src} (copy)"
     else:
-        achieved, peak, unit = amount / sec / 1e12, tflops, "TFLOP/s"
+        achieved, peak, unit = amount / sec / 1e12, alu_peak / 1e12, "TFLOP/s (fp32 ALU)"
+        peak_note = f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {MAX_SM_MHZ:.0f} MHz"
     t_roof = max(total_bytes / (hbm * 1e9), ops / (tflops * 1e12))
+    t_alu = alu_partials(cfg, R) * ALU_OPS_PER_PARTIAL[cfg.wtype] / alu_peak
     qs_sec = mean_stage[1] / 1e3
     qs_gbs = stages["quantize_scatter"][1] / qs_sec / 1e9
     value = weak_scaling_value(world, T, ms)
@@ -386,13 +419,21 @@ def run_gpu(args, rank, world, local_rank):
         "config": dict(cfg.describe(), l2="flushed between steps (512 MB write)",
                        n_active_experts=n_active, mmq_path=mmq_path()),
         "roofline": {"kernel": dom_name, "bound": bound, "achieved": round(achieved, 2),
-                     "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
+                     "peak": round(peak, 2), "unit": unit, "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(dom_name, cfg.name),
-                     "peak_source": f"{peak_src} ({'sustained' if bound == 'tensor' else 'copy'})"},
+                     "peak_source": peak_note},
+        **({"roofline_tensor": {
+            "kernel": dom_name, "achieved": round(mmq_tensor_flops(cfg, R, dom_name) / sec / 1e12, 2),
+            "peak": tflops, "unit": "TFLOP/s (block dots)",
+            "frac": round(mmq_tensor_flops(cfg, R, dom_name) / sec / 1e12 / tflops, 4),
+            "peak_source": f"{peak_src} (sustained bf16; the fp16 MMA runs at the bf16 rate)"}}
+           if bound == "alu" else {}),
         "layer_roofline": {"t_roofline_ms": round(t_roof * 1e3, 4),
                            "frac": round(t_roof * 1e3 / ms, 4),
                            "algorithmic_bytes": int(total_bytes), "ops": ops,
-                           "bound": "hbm" if total_bytes / hbm / 1e9 >= ops / tflops / 1e12 else "tensor"},
+                           "bound": "hbm" if total_bytes / hbm / 1e9 >= ops / tflops / 1e12 else "tensor",
+                           "alu_floor_ms": round(t_alu * 1e3, 4),
+                           "frac_of_alu_floor": round(t_alu * 1e3 / ms, 4)},
         "quantize_scatter": {"GB/s": round(qs_gbs, 1), "frac_of_hbm": round(qs_gbs / hbm, 4),
                              "bytes": int(stages["quantize_scatter"][1])},
         "phases_ms": phases,
@@ -404,12 +445,88 @@ def run_gpu(args, rank, world, local_rank):
         "wall_s_timed": round(t_wall, 3),
         "clocks": clocks,
     }
+    if not args.no_ab:
+        # after the timed region: these calls reuse the layer's buffers
+        line["ab"] = ab_compare(m, layer, x, ids, flush, K)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
     return line
+
+
+def ab_compare(m, layer, x, ids, flush, K, reps: int = 10):
+    """The pages' own comparisons on this GPU, each checked for byte identity:
+    per-row gather quantization (each token row quantized again for each of its
+    K expert rows) against quantize-once-and-scatter, and the expert gather as
+    one launch per expert, one per group of 16, and one device-driven launch."""
+    import torch
+
+    L = layer
+    T, d = x.shape
+    R = T * K
+    E = L.E
+    m.moe_build_slot_map(ids, E, L.offsets, L.slot, L.src, L.active, L.n_active, L.ws)
+    torch.cuda.synchronize()
+    n_active = int(L.n_active.item())
+    active = L.active[:n_active].cpu().tolist()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        tot = 0.0
+        for i in range(reps):
+            flush.fill_(i & 0xFF)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / reps
+
+    q2, ds2 = torch.empty_like(L.q), torch.empty_like(L.ds)
+    t_scatter = timed(lambda: m.moe_quantize_scatter_q8_1(x, L.slot, K, R, L.q, L.ds))
+    t_gather = timed(lambda: m.moe_quantize_gather_q8_1(x, L.src, R, q2, ds2))
+    q_same = bool(torch.equal(L.q[:R], q2[:R]) and torch.equal(L.ds[:R], ds2[:R]))
+
+    ss = L.slot_stride
+    used = n_active * ss
+
+    def per_expert():
+        for p, e in enumerate(active):
+            base = (p // 16) * 16 * ss
+            m.moe_group_gather(L.arena, L.rec_bytes, L.arena_stride, [e], p % 16,
+                               L.group_buf[base:], ss)
+
+    def per_group():
+        for g0 in range(0, n_active, 16):
+            m.moe_group_gather(L.arena, L.rec_bytes, L.arena_stride, active[g0:g0 + 16], 0,
+                               L.group_buf[g0 * ss:], ss)
+
+    def device():
+        m.moe_group_gather_active(L.arena, L.rec_bytes, L.arena_stride, L.active, L.n_active, E,
+                                  L.group_buf, ss)
+
+    t_dev = timed(device)
+    ref = L.group_buf[:used].clone()
+    t_group = timed(per_group)
+    same_group = bool(torch.equal(L.group_buf[:used], ref))
+    t_expert = timed(per_expert)
+    same_expert = bool(torch.equal(L.group_buf[:used], ref))
+    return {
+        "quantize": {"scatter_ms": round(t_scatter, 4), "per_row_gather_ms": round(t_gather, 4),
+                     "gather_over_scatter": round(t_gather / t_scatter, 3),
+                     "bytes_identical": q_same},
+        "group_gather": {"n_active_experts": n_active,
+                         "one_device_launch_ms": round(t_dev, 4),
+                         "per_group_of_16_ms": round(t_group, 4),
+                         "per_group_launches": (n_active + 15) // 16,
+                         "per_expert_ms": round(t_expert, 4), "per_expert_launches": n_active,
+                         "bytes_identical": same_group and same_expert},
+    }
 
 
 def mmq_path() -> str:
@@ -496,9 +613,14 @@ def _time_stage(args, cfg, fn, ws, n_active, rec_bytes):
     bound, amount = stages[args.stage]
     t = float(np.mean(ms)) / 1e3
     rate = amount / t / (1e9 if bound == "hbm" else 1e12)
-    return {"stage": args.stage, "config": cfg.describe(), "ms": round(t * 1e3, 4),
-            "bound": bound, "achieved": round(rate, 2),
-            "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "n_active_experts": n_active}
+    out = {"stage": args.stage, "config": cfg.describe(), "ms": round(t * 1e3, 4),
+           "bound": bound, "achieved": round(rate, 2),
+           "unit": "GB/s" if bound == "hbm" else "TFLOP/s (fp32 ALU)", "n_active_experts": n_active}
+    if bound == "alu":
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        out["frac"] = round(rate * 1e12 / alu_peak_ops(sms), 4)
+        out["tensor_tflops"] = round(mmq_tensor_flops(cfg, cfg.T * cfg.K, args.stage) / t / 1e12, 2)
+    return out
 
 
 # ------------------------------------------------------------- CPU oracle --
@@ -570,6 +692,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ab", action="store_true",
+                    help="skip the gather-quantization and per-expert gather comparisons")
     ap.add_argument("--stage", default=None,
                     help="time one stage alone (for profiler captures): quantize_scatter, "
                          "mmq_gateup, mmq_down, requant_hidden, combine_topk, group_gather")
