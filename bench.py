@@ -448,12 +448,48 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_ab:
         # after the timed region: these calls reuse the layer's buffers
         line["ab"] = ab_compare(m, layer, x, ids, flush, K)
+    if args.streamed:
+        line["streamed"] = streamed_measure(m, layer, wl, x, ids, w, flush, args, ms, n_active)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
     return line
+
+
+def streamed_measure(m, layer, wl, x, ids, w, flush, args, resident_ms, n_active):
+    """The layer with the expert records in pinned host memory, streamed over
+    NVLink-C2C through the device staging ring: per-step time (CUDA events on
+    the compute stream, the call's own synchronization included) and the
+    host-to-device bytes it moved."""
+    import torch
+
+    host_arena = torch.from_numpy(wl.arena).pin_memory()
+
+    def step():
+        layer.forward_streamed(host_arena, x, ids, w, ring_groups=args.ring_groups)
+
+    for _ in range(max(2, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    assert m.moe_device_error(layer.ws) == 0
+    t = float(np.mean(times))
+    h2d = n_active * wl.rec_bytes
+    return {"ms_per_step": round(t, 4), "tokens/s": round(wl.cfg.T / t * 1e3, 1),
+            "ring_groups": args.ring_groups, "h2d_bytes_per_step": int(h2d),
+            "h2d_GB/s_over_step": round(h2d / t / 1e6, 1),
+            "vs_resident_ms": round(t / resident_ms, 3)}
 
 
 def ab_compare(m, layer, x, ids, flush, K, reps: int = 10):
@@ -692,6 +728,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--streamed", action="store_true",
+                    help="also time the layer with the expert records streamed from pinned host memory")
+    ap.add_argument("--ring-groups", type=int, default=3)
     ap.add_argument("--no-ab", action="store_true",
                     help="skip the gather-quantization and per-expert gather comparisons")
     ap.add_argument("--stage", default=None,

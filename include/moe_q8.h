@@ -23,8 +23,9 @@
  *
  * Conventions shared by every call:
  *   - Pointers are DEVICE pointers owned by the caller unless a parameter says
- *     "host".  No call allocates, frees, synchronizes (except moe_device_error)
- *     or keeps a pointer after it returns.  Every call is asynchronous on
+ *     "host".  No call allocates, frees, synchronizes (except moe_device_error
+ *     and moe_layer_forward_streamed, which say what they do) or keeps a
+ *     pointer after it returns.  Every call is asynchronous on
  *     `stream` (a cudaStream_t; NULL = the legacy default stream).
  *   - Misuse that the host can see (null pointer with nonzero size, a width that
  *     is not a multiple of 32, a misaligned buffer, too small a workspace, a
@@ -232,6 +233,62 @@ int moe_combine_topk(const float* y, int R, const int32_t* slot, const float* w,
 int moe_build_slot_map_noalloc(const int32_t* ids, int T, int K, int E, int32_t* offsets,
                                int32_t* slot, int32_t* src, int32_t* active, int32_t* n_active,
                                void* stream);
+
+/*
+ * The whole layer with the expert records in HOST memory (pinned, for example
+ * from cudaHostAlloc), streamed to the GPU as the pull-request pages' streamed
+ * walk does ([#372] "What changes"; [#439] "Ring-slot safety"):
+ *   - copy_stream: each routed expert's record, in ascending id order, is copied
+ *     (one cudaMemcpyAsync per record) into the next slot of a device staging
+ *     ring of ring_groups x 16 slots; before refilling a slot the copy stream
+ *     waits on the event that last released it; a group's last copy records
+ *     the group's "staged" event;
+ *   - compute_stream: per group of 16 routed experts, one wait on "staged", one
+ *     gather launch from the ring into the 16-slot MMQ group buffer, one event
+ *     that releases all of the group's ring slots, then the group's stage 4, 5
+ *     and 6 calls; stage 7 once at the end.
+ * Stages 1-2 run first on compute_stream; the call then synchronizes it once to
+ * read the routed experts and their row offsets into b->host_scratch, and
+ * returns after enqueuing the rest (asynchronous from there).  The output is
+ * bit-identical to the resident layer's (the same kernels on the same bytes).
+ * The library pairs 2 x 64 CUDA events with each device on first use and keeps
+ * them for the process; calls on one device that overlap must not share a
+ * ring_groups slice of them, so run them one after another.
+ *   - host_arena: host pointer, record e at e * arena_stride (rec_bytes each).
+ *   - ring: device, ring_groups * 16 * slot_stride bytes; group_buf: device,
+ *     16 * slot_stride bytes (128-byte aligned, slot_stride % 128 == 0);
+ *     group_counts: device int32 [ceil(E / 16)];
+ *     host_scratch: host int32 [2 * E + 2].
+ *   - The other buffers as the stage calls document (q, ds for T*K rows of d;
+ *     h, hq, hds for T*K rows of f; y for T*K rows of d; ws of
+ *     moe_workspace_size(T, K, E, d, f) bytes).
+ *   - ring_groups in [1, 64]; compute_stream != copy_stream.
+ */
+typedef struct moe_stream_buffers {
+    uint8_t* ring;
+    uint8_t* group_buf;
+    int32_t* group_counts;
+    int32_t* offsets;
+    int32_t* slot;
+    int32_t* src;
+    int32_t* active;
+    int32_t* n_active;
+    int8_t* q;
+    uint16_t* ds;
+    float* h;
+    int8_t* hq;
+    uint16_t* hds;
+    float* y;
+    void* ws;
+    size_t ws_bytes;
+    int32_t* host_scratch;
+} moe_stream_buffers;
+
+int moe_layer_forward_streamed(int wtype, int T, int K, int E, int d, int f, const float* x,
+                               const int32_t* ids, const float* w, float* out,
+                               const uint8_t* host_arena, size_t rec_bytes, size_t arena_stride,
+                               size_t slot_stride, int ring_groups, const moe_stream_buffers* b,
+                               void* compute_stream, void* copy_stream);
 
 /* Synchronize `stream`, read the workspace error word into *bits (host) and
    clear it.  Returns MOE_ERR_DEVICE if any bit was set, MOE_OK otherwise. */

@@ -50,6 +50,8 @@ _SIGNATURES = {
     "moe_grouped_mmq_down": (_I, [_I, _P, _Z, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_combine_topk": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
     "moe_build_slot_map_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "moe_layer_forward_streamed": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _Z, _Z,
+                                        _I, _P, _P, _P]),
     "moe_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_launch_count": (ctypes.c_ulonglong, []),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -208,6 +210,31 @@ def moe_build_slot_map_noalloc(ids, E, offsets, slot, src, active, n_active, str
            "moe_build_slot_map_noalloc")
 
 
+class StreamBuffers(ctypes.Structure):
+    """moe_stream_buffers: the device (and one host) buffers of the streamed layer."""
+    _fields_ = [(n, _P) for n in ("ring", "group_buf", "group_counts", "offsets", "slot", "src",
+                                  "active", "n_active", "q", "ds", "h", "hq", "hds", "y", "ws")]
+    _fields_ += [("ws_bytes", _Z), ("host_scratch", _P)]
+
+
+def moe_layer_forward_streamed(wtype, x, ids, w, out, host_arena, rec_bytes, arena_stride,
+                               slot_stride, ring_groups, bufs: "StreamBuffers", E, f,
+                               compute_stream=None, copy_stream=None):
+    """The whole layer with the expert records in host memory (host_arena: a
+    pinned CPU uint8 tensor), streamed through the device ring in bufs."""
+    _dev(x, ids, w, out)
+    if host_arena.is_cuda:
+        raise ValueError("host_arena must be a (pinned) host tensor")
+    T, d = x.shape
+    K = ids.shape[1]
+    _check(lib().moe_layer_forward_streamed(wtype, T, K, E, d, f, _p(x), _p(ids), _p(w), _p(out),
+                                            ctypes.c_void_p(host_arena.data_ptr()), rec_bytes,
+                                            arena_stride, slot_stride, ring_groups,
+                                            ctypes.byref(bufs), _s(compute_stream),
+                                            _s(copy_stream)),
+           "moe_layer_forward_streamed")
+
+
 def moe_device_error(ws, stream=None) -> int:
     """Synchronize the stream and return (and clear) the workspace error bits."""
     bits = ctypes.c_uint32(0)
@@ -275,3 +302,32 @@ class MoeLayer:
                              self.ws, stream)
         moe_combine_topk(self.y, R, self.slot, w, T, K, d, self.out, stream)
         return self.out[:T]
+
+    def forward_streamed(self, host_arena, x, ids, w, ring_groups=3, stream=None):
+        """As forward, with the expert records read from host_arena (pinned host
+        memory, record e at e*arena_stride) and streamed through a device ring of
+        ring_groups x 16 slots on a copy stream of the layer's own."""
+        dev = self.group_buf.device
+        if getattr(self, "_ring_groups", None) != ring_groups:
+            self.ring = torch.zeros(ring_groups * 16 * self.slot_stride, dtype=torch.uint8,
+                                    device=dev)
+            self._ring_groups = ring_groups
+        if not hasattr(self, "stage_buf"):
+            self.stage_buf = torch.zeros(16 * self.slot_stride, dtype=torch.uint8, device=dev)
+            self.group_counts = torch.zeros((self.E + 15) // 16, dtype=torch.int32, device=dev)
+            self.host_scratch = torch.zeros(2 * self.E + 2, dtype=torch.int32).pin_memory()
+            self.copy_stream = torch.cuda.Stream(device=dev)
+        b = StreamBuffers()
+        for name, t in (("ring", self.ring), ("group_buf", self.stage_buf),
+                        ("group_counts", self.group_counts), ("offsets", self.offsets),
+                        ("slot", self.slot), ("src", self.src), ("active", self.active),
+                        ("n_active", self.n_active), ("q", self.q), ("ds", self.ds),
+                        ("h", self.h), ("hq", self.hq), ("hds", self.hds), ("y", self.y),
+                        ("ws", self.ws), ("host_scratch", self.host_scratch)):
+            setattr(b, name, t.data_ptr())
+        b.ws_bytes = self.ws.numel()
+        cs = stream if stream is not None else torch.cuda.current_stream(dev)
+        moe_layer_forward_streamed(self.wtype, x, ids, w, self.out, host_arena, self.rec_bytes,
+                                   self.arena_stride, self.slot_stride, ring_groups, b, self.E,
+                                   self.f, cs, self.copy_stream)
+        return self.out[:x.shape[0]]

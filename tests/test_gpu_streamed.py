@@ -1,0 +1,62 @@
+"""GPU: the layer with the expert records in pinned host memory, streamed through
+the device staging ring (moe_layer_forward_streamed), against the resident layer.
+
+The streamed walk runs the same kernels on the same bytes, group by group, so
+its output must equal the resident layer's bit for bit; the ring sizes below
+force slot reuse (a ring of one to three groups for up to 32 groups of experts),
+which exercises the copy stream's waits on the events that release ring slots.
+"""
+import numpy as np
+import pytest
+
+import moe_workloads as mw
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import quantized_routed_expert_q8_gb300 as m  # noqa: E402
+
+
+def _layer(wl):
+    cfg = wl.cfg
+    return m.MoeLayer(cfg.wtype, cfg.E, cfg.d, cfg.f, cfg.K, cfg.T, H.to_dev(wl.arena),
+                      wl.rec_bytes, wl.arena_stride)
+
+
+@pytest.mark.parametrize("name,ring_groups", [(mw.TINY.name, 1), (mw.T600.name, 1),
+                                              (mw.T600.name, 3), (mw.T2048.name, 2)])
+def test_streamed_equals_resident(name, ring_groups):
+    wl = H.workload(name)
+    layer = _layer(wl)
+    x, ids, w = H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w)
+    ref = layer.forward(x, ids, w).clone()
+    assert m.moe_device_error(layer.ws) == 0
+    host_arena = torch.from_numpy(wl.arena).pin_memory()
+    layer.out.fill_(float("nan"))
+    layer.y.fill_(float("nan"))
+    got = layer.forward_streamed(host_arena, x, ids, w, ring_groups=ring_groups)
+    torch.cuda.synchronize()
+    assert m.moe_device_error(layer.ws) == 0
+    assert torch.equal(got, ref)
+    # and again, reusing the events and the ring
+    got2 = layer.forward_streamed(host_arena, x, ids, w, ring_groups=ring_groups).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(got2, ref)
+
+
+def test_streamed_rejects_bad_arguments():
+    wl = H.workload(mw.TINY.name)
+    layer = _layer(wl)
+    x, ids, w = H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w)
+    with pytest.raises(ValueError):  # a device tensor is not a host arena
+        layer.forward_streamed(layer.arena, x, ids, w)
+    host_arena = torch.from_numpy(wl.arena).pin_memory()
+    with pytest.raises(m.MoeError):
+        layer.forward_streamed(host_arena, x, ids, w, ring_groups=0)
+    with pytest.raises(m.MoeError):
+        layer.forward_streamed(host_arena, x, ids, w, ring_groups=65)
+    assert np.isfinite(layer.forward_streamed(host_arena, x, ids, w).cpu().numpy()).all()
