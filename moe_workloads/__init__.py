@@ -14,8 +14,9 @@ Recipe (all seeded, counter-based, independent of thread count):
   w      = softmax over the K selected logits, in float64, stored fp32.
   weights: gate/up [f, d], down [d, f] per expert ~ N(0, 0.02) (tensor id
            100 + 3e + m), quantized per 32-wide block of the reduction dimension
-           to Q8_0 (d = amax/127, q = round(w/d)) or Q4_1 (d = (max-min)/15,
-           m = min, q = round((w-m)/d) clamped to [0, 15]); scales stored fp16.
+           to Q8_0 (d = amax/127, q = round(w/d)), Q4_1 (d = (max-min)/15,
+           m = min, q = round((w-m)/d) clamped to [0, 15]) or Q2_0 (d = amax/2,
+           c = round(w/d) + 2 clamped to [0, 3]); scales stored fp16.
 """
 from __future__ import annotations
 
@@ -33,7 +34,8 @@ LIB = os.path.join(HERE, "libmoe_gen.so")
 
 Q8_0 = 0
 Q4_1 = 1
-WTYPE_NAMES = {Q8_0: "q8_0", Q4_1: "q4_1"}
+Q2_0 = 2
+WTYPE_NAMES = {Q8_0: "q8_0", Q4_1: "q4_1", Q2_0: "q2_0"}
 
 _lock = threading.Lock()
 _lib = None
@@ -145,9 +147,11 @@ CONFIGS = {c.name: c for c in [
            routing="zipf"),
     Config("T32768_d2048_f768_E512_K10_q4_1", 32768, 2048, 768, 512, 10, Q4_1, 0x5EED0005,
            zero_every=997),
+    Config("T2048_d2048_f768_E512_K10_q2_0", 2048, 2048, 768, 512, 10, Q2_0, 0x5EED0006,
+           zero_tokens=(1024,)),
 ]}
 CONFIG_LIST = list(CONFIGS.values())
-TINY, T600, T2048, T8192, T32768 = CONFIG_LIST
+TINY, T600, T2048, T8192, T32768, T2048_Q2 = CONFIG_LIST
 
 
 def routing_logits(cfg: Config, tokens: np.ndarray | None = None) -> np.ndarray:

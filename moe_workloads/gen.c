@@ -111,11 +111,11 @@ void gen_normal_f32(uint64_t seed, uint64_t tensor_id, uint64_t start, size_t n,
 /* ---------------- expert records (the library's weight format) --------------- */
 /* gate [f x d], up [f x d], down [d x f]; per matrix: quant plane, fp16 d plane
    [K/32][rows] (block-major), Q4_1 also fp16 m plane [K/32][rows]; planes
-   128-byte aligned. */
+   128-byte aligned.  Quant bytes per row: K (Q8_0), K/2 (Q4_1), K/4 (Q2_0). */
 static size_t a128(size_t x) { return (x + 127u) & ~(size_t)127u; }
 
 static size_t mat_bytes(int wtype, int rows, int k, size_t* qoff, size_t* doff, size_t* moff) {
-    size_t qb = (size_t)rows * (size_t)k / (wtype == 1 ? 2u : 1u);
+    size_t qb = (size_t)rows * (size_t)k / (wtype == 1 ? 2u : wtype == 2 ? 4u : 1u);
     size_t sb = (size_t)rows * (size_t)(k / 32) * 2u;
     *qoff = 0;
     *doff = a128(qb);
@@ -155,6 +155,21 @@ static void pack_matrix(int wtype, const float* w, int rows, int k, uint8_t* dst
                     float x = dd > 0.0f ? roundf(v[i] / dd) : 0.0f;
                     x = fminf(127.0f, fmaxf(-127.0f, x));
                     q[i] = (int8_t)x;
+                }
+                dp[(size_t)b * rows + r] = to_f16_bits(dd);
+            } else if (wtype == 2) { /* Q2_0: d = amax/2, c = round(w/d) + 2 in [0,3] */
+                float amax = 0.0f;
+                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+                float dd = amax / 2.0f;
+                uint8_t* q = qp + (size_t)r * (k / 4) + (size_t)b * 8;
+                for (int j = 0; j < 8; ++j) {
+                    uint8_t byte = 0;
+                    for (int i = 0; i < 4; ++i) {
+                        float x = dd > 0.0f ? roundf(v[4 * j + i] / dd) : 0.0f;
+                        x = fminf(1.0f, fmaxf(-2.0f, x));
+                        byte |= (uint8_t)(((int)x + 2) << (2 * i));
+                    }
+                    q[j] = byte;
                 }
                 dp[(size_t)b * rows + r] = to_f16_bits(dd);
             } else { /* Q4_1: d = (max-min)/15, m = min, q = round((w-m)/d) in [0,15] */

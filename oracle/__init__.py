@@ -24,6 +24,7 @@ LIB = os.path.join(HERE, "liboracle.so")
 
 W_Q8_0 = 0
 W_Q4_1 = 1
+W_Q2_0 = 2
 QK = 32
 
 _lock = threading.Lock()

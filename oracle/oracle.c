@@ -33,6 +33,12 @@
  *   Q4_1 weights:     32-wide blocks, 4-bit unsigned q (two per byte: byte j holds
  *                     element 2j in its low nibble, 2j+1 in its high nibble),
  *                     fp16 d and fp16 m, w = d*q + m; the MMQ uses s for the m term.
+ *   Q2_0 weights:     named by "#1368 ..." (section "Identity": the D4 activation
+ *                     layout serves Q2_0, Q8_0 and IQ2_XS) but not defined there;
+ *                     this library's definition: 32-wide blocks, 2-bit codes c
+ *                     (four per byte: element 4j+i of a block in bits 2i..2i+1 of
+ *                     byte j), fp16 d, w = d*(c - 2), so the block dot uses the
+ *                     integers c - 2 in {-2, -1, 0, 1} and no m term.
  *   Gate/up product:  h = SiLU(g) * u with SiLU(g) = g / (1 + exp(-g)).
  *
  * Parity pins for every function are in tests/test_oracle_pins.py.
@@ -43,9 +49,14 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define QK 32 /* block width of q8_1, Q8_0 and Q4_1 */
+#define QK 32 /* block width of q8_1, Q8_0, Q4_1 and Q2_0 */
 
-enum { ORACLE_W_Q8_0 = 0, ORACLE_W_Q4_1 = 1 };
+enum { ORACLE_W_Q8_0 = 0, ORACLE_W_Q4_1 = 1, ORACLE_W_Q2_0 = 2 };
+
+/* quant bytes per row of a matrix with reduction length k */
+static size_t quant_row_bytes(int wtype, int k) {
+    return (size_t)k / (wtype == ORACLE_W_Q4_1 ? 2u : wtype == ORACLE_W_Q2_0 ? 4u : 1u);
+}
 
 /* ------------------------------------------------------------------------- */
 /* IEEE 754 binary16 conversion, written from the format's definition:        */
@@ -128,7 +139,7 @@ typedef struct {
 
 static oracle_matrix_layout matrix_layout(int wtype, int rows, int k) {
     oracle_matrix_layout L;
-    size_t qbytes = (size_t)rows * (size_t)k / (wtype == ORACLE_W_Q4_1 ? 2u : 1u);
+    size_t qbytes = (size_t)rows * quant_row_bytes(wtype, k);
     size_t sbytes = (size_t)rows * (size_t)(k / QK) * 2u;
     L.q = 0;
     L.d = align128(qbytes);
@@ -301,6 +312,12 @@ static float mmq_dot(int wtype, const uint8_t* wq_row, const uint16_t* wd, const
         if (wtype == ORACLE_W_Q8_0) {
             const int8_t* wb = (const int8_t*)wq_row + b * QK;
             for (int i = 0; i < QK; ++i) I += (int32_t)wb[i] * (int32_t)xb[i];
+        } else if (wtype == ORACLE_W_Q2_0) {
+            const uint8_t* wb = wq_row + b * (QK / 4);
+            for (int i = 0; i < QK; ++i) {
+                int32_t c = (wb[i / 4] >> (2 * (i % 4))) & 3;
+                I += (c - 2) * (int32_t)xb[i];
+            }
         } else {
             const uint8_t* wb = wq_row + b * (QK / 2);
             for (int j = 0; j < QK / 2; ++j) {
@@ -331,7 +348,7 @@ static wmat weight_matrix(int wtype, const uint8_t* base, int rows, int k) {
     W.q = base + L.q;
     W.d = (const uint16_t*)(base + L.d);
     W.m = (const uint16_t*)(base + L.m);
-    W.q_row = (size_t)k / (wtype == ORACLE_W_Q4_1 ? 2u : 1u);
+    W.q_row = quant_row_bytes(wtype, k);
     W.rows = rows;
     return W;
 }

@@ -251,14 +251,24 @@ def test_group_gather_equals_one_copy_per_expert(rec, arena_off):
 
 # --------------------------------------------------------------------- MMQ ---
 
+def _qbytes(wtype, rows, k):
+    return rows * k // {mw.Q8_0: 1, mw.Q4_1: 2, mw.Q2_0: 4}[wtype]
+
+
 def _planes(wtype, rec, off, rows, k):
-    """Decode one matrix of a record with numpy (independent of the oracle)."""
-    qb = rows * k // (2 if wtype == mw.Q4_1 else 1)
+    """Decode one matrix of a record with numpy (independent of the oracle).
+    Q2_0 codes come back as their values c - 2."""
+    qb = _qbytes(wtype, rows, k)
     a128 = lambda v: (v + 127) // 128 * 128
     sb = rows * (k // 32) * 2
     base = rec[off:]
     if wtype == mw.Q8_0:
         q = base[:qb].view(np.int8).reshape(rows, k).astype(np.int64)
+    elif wtype == mw.Q2_0:
+        p = base[:qb].reshape(rows, k // 4).astype(np.int64)
+        q = np.empty((rows, k), np.int64)
+        for i in range(4):  # element 4j+i sits in bits 2i..2i+1 of byte j
+            q[:, i::4] = ((p >> (2 * i)) & 3) - 2
     else:
         p = base[:qb].reshape(rows, k // 2)
         q = np.empty((rows, k), np.int64)
@@ -287,7 +297,7 @@ def _dequant_x(q, ds):
 
 def _mat_offsets(wtype, d, f):
     a128 = lambda v: (v + 127) // 128 * 128
-    qb = f * d // (2 if wtype == mw.Q4_1 else 1)
+    qb = _qbytes(wtype, f, d)
     sb = f * (d // 32) * 2
     g = a128(qb) + a128(sb) * (2 if wtype == mw.Q4_1 else 1)
     return 0, g, 2 * g
@@ -298,7 +308,7 @@ def _silu_mul64(g, u):
         return g / (1.0 + np.exp(-g)) * u
 
 
-@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1])
+@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0])
 def test_record_layout_agrees(wtype):
     for d, f in ((256, 128), (2048, 768), (96, 64)):
         assert oracle.expert_record_bytes(wtype, d, f) == mw.record_bytes(wtype, d, f)
@@ -306,6 +316,8 @@ def test_record_layout_agrees(wtype):
     # sizes worked out by hand: 3*f*d*34/32 and 3*f*d*20/32 at d=2048, f=768
     assert oracle.expert_record_bytes(mw.Q8_0, 2048, 768) == 5013504
     assert oracle.expert_record_bytes(mw.Q4_1, 2048, 768) == 2949120
+    # Q2_0: 3*f*d*(2/8 + 2/32)
+    assert oracle.expert_record_bytes(mw.Q2_0, 2048, 768) == 1474560
 
 
 def _small_problem(wtype, T=9, d=128, f=96, E=5, K=2, seed=11):
@@ -316,7 +328,7 @@ def _small_problem(wtype, T=9, d=128, f=96, E=5, K=2, seed=11):
     return arena, rb, stride, x, ids, w
 
 
-@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1])
+@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0])
 def test_mmq_against_dequantized_matmul(wtype):
     """The block-scaled integer dot equals the product of the dequantized
     matrices (w = d*q (+m), x = d_x*q_x), computed by a plain fp64 matmul.  For
@@ -458,9 +470,42 @@ def test_combine_closed_forms():
     assert np.allclose(out2, oracle.combine_topk(y, slot, w2, T, K, d), rtol=0, atol=1e-6)
 
 
+def test_mmq_q2_0_integer_special_case():
+    """Q2_0 with every scale 1: the down product is exactly the integer matrix
+    product with the weights c - 2, codes packed here by hand (element 4j+i in
+    bits 2i..2i+1 of byte j), which pins the code order and the offset."""
+    d, f, E = 64, 96, 2
+    rng = np.random.default_rng(7)
+    rb = oracle.expert_record_bytes(mw.Q2_0, d, f)
+    og, ou, od = _mat_offsets(mw.Q2_0, d, f)
+    recs = np.zeros(E * rb, np.uint8)
+    Wd = []
+    for e in range(E):
+        c = rng.integers(0, 4, (d, f))
+        Wd.append(c - 2)
+        packed = np.zeros((d, f // 4), np.uint8)
+        for j in range(f // 4):
+            for i in range(4):
+                packed[:, j] |= (c[:, 4 * j + i] << (2 * i)).astype(np.uint8)
+        base = e * rb + od
+        recs[base:base + d * f // 4] = packed.ravel()
+        dpl = np.full(d * (f // 32), 0x3C00, np.uint16).view(np.uint8)
+        o = base + ((d * f // 4 + 127) // 128) * 128
+        recs[o:o + dpl.size] = dpl
+    R = 9
+    hq = rng.integers(-127, 128, (R, f)).astype(np.int8)
+    hds = np.zeros((R, f // 32, 2), np.uint16)
+    hds[..., 0] = 0x3C00
+    offsets = np.array([0, 4, 9], np.int32)
+    active = np.array([0, 1], np.int32)
+    y = oracle.grouped_mmq_down(mw.Q2_0, recs, rb, active, 2, offsets, hq, hds, d, f)
+    ref = np.concatenate([hq[0:4].astype(np.int64) @ Wd[0].T, hq[4:9].astype(np.int64) @ Wd[1].T])
+    assert np.array_equal(y.astype(np.float64), ref.astype(np.float64))
+
+
 # ------------------------------------------------------------ end to end ---
 
-@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1])
+@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0])
 def test_layer_end_to_end_tiny(wtype):
     """Tiny layer: the all-zero token gives an exactly zero row, and the whole
     layer agrees with an unquantized fp64 pipeline (dequantized weights, raw
