@@ -170,7 +170,7 @@ def pci_bus_id(dev):
 
 # FP32 operations per block-scale partial in the MMQ epilogue: fma(dW*dX, I, acc)
 # is a multiply and an FMA; Q4_1 adds fma(mW, sX, acc).
-ALU_OPS_PER_PARTIAL = {0: 2, 1: 3}  # by weight type (0 Q8_0, 1 Q4_1)
+ALU_OPS_PER_PARTIAL = {0: 2, 1: 3, 2: 2}  # by weight type (Q8_0, Q4_1, Q2_0)
 FP32_LANES_PER_SM = 128
 MAX_SM_MHZ = 2070.0  # GB300 maximum SM clock
 

@@ -47,11 +47,14 @@
  *   Expert record (this library's layout): three matrices, gate [f x d], up
  *     [f x d], down [d x f], each stored as: quant plane (rows x K, reduction
  *     dimension innermost; Q8_0 int8; Q4_1 two 4-bit values per byte, byte j of
- *     a block holding element 2j in the low nibble and 2j+1 in the high), then
- *     the binary16 d plane [K/32][rows] (block-major: the scale of row j, block
- *     b is entry b*rows + j), then for Q4_1 the binary16 m plane [K/32][rows].
- *     Every plane starts on a 128-byte boundary.  Weight value w = d*q (Q8_0)
- *     or d*q + m (Q4_1).
+ *     a block holding element 2j in the low nibble and 2j+1 in the high; Q2_0
+ *     four 2-bit codes per byte, byte j of a block holding element 4j+i in bits
+ *     2i..2i+1), then the binary16 d plane [K/32][rows] (block-major: the scale
+ *     of row j, block b is entry b*rows + j), then for Q4_1 the binary16 m plane
+ *     [K/32][rows].  Every plane starts on a 128-byte boundary.  Weight value
+ *     w = d*q (Q8_0), d*q + m (Q4_1) or d*(c - 2) (Q2_0, code c in 0..3).  The
+ *     pages name Q2_0 ([#1368] "Identity") without defining it; this is the
+ *     library's own definition.
  */
 #ifndef MOE_Q8_H
 #define MOE_Q8_H
@@ -73,7 +76,7 @@ typedef enum {
     MOE_ERR_DEVICE = -6       /* moe_device_error found a device-side error bit */
 } moe_status;
 
-typedef enum { MOE_W_Q8_0 = 0, MOE_W_Q4_1 = 1 } moe_wtype;
+typedef enum { MOE_W_Q8_0 = 0, MOE_W_Q4_1 = 1, MOE_W_Q2_0 = 2 } moe_wtype;
 
 /* Device error bits, set in the workspace error word. */
 #define MOE_DEV_ERR_BAD_EXPERT_ID 0x1u /* an id outside [0, E): its slot is -1 */

@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(HERE, "libmoe_q8.so")
 
 MOE_W_Q8_0 = 0
 MOE_W_Q4_1 = 1
+MOE_W_Q2_0 = 2
 QK = 32
 
 DEV_ERR_BAD_EXPERT_ID = 0x1

@@ -43,7 +43,7 @@ namespace {
 
 inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline bool al(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
-inline bool wtype_ok(int w) { return w == MOE_W_Q8_0 || w == MOE_W_Q4_1; }
+inline bool wtype_ok(int w) { return w == MOE_W_Q8_0 || w == MOE_W_Q4_1 || w == MOE_W_Q2_0; }
 
 // MOE_MMQ_PATH=simt forces the CUDA-core MMQ (cross-check of the tensor-core path)
 inline bool force_simt() {

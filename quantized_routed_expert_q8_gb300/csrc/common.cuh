@@ -11,7 +11,12 @@
 
 namespace moe {
 
-constexpr int QK = 32;  // block width of q8_1, Q8_0 and Q4_1
+constexpr int QK = 32;  // block width of q8_1, Q8_0, Q4_1 and Q2_0
+
+// quant bytes per row of a weight matrix with reduction length k
+__host__ __device__ inline size_t quant_row_bytes(int wtype, int k) {
+    return (size_t)k / (wtype == MOE_W_Q4_1 ? 2 : wtype == MOE_W_Q2_0 ? 4 : 1);
+}
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -25,7 +30,7 @@ struct MatLayout {
 
 __host__ __device__ inline MatLayout mat_layout(int wtype, int rows, int k) {
     MatLayout L;
-    size_t qb = (size_t)rows * (size_t)k / (wtype == MOE_W_Q4_1 ? 2 : 1);
+    size_t qb = (size_t)rows * quant_row_bytes(wtype, k);
     size_t sb = (size_t)rows * (size_t)(k / QK) * 2;
     L.q = 0;
     L.d = align_up(qb, 128);

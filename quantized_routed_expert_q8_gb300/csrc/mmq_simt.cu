@@ -5,6 +5,7 @@
 // For the expert at active position p and each of its rows r:
 //   acc = sum over 32-blocks b ascending of
 //         fma(fp32(dW[j,b]) * fp32(dx[r,b]), I_b, acc)  (+ fma(mW[j,b], sx[r,b], acc) for Q4_1)
+// (Q2_0: the block dot uses the weight integers c - 2)
 // with I_b the exact int32 block dot -- the same fp32 operation sequence as the
 // scalar definition, so the result does not depend on the tiling.
 // Tile: 64 rows x 64 output columns per block of 256 threads, one 32-block of
@@ -22,6 +23,12 @@ __device__ __forceinline__ void unpack_q4_pair(uint32_t bytes2, uint32_t& w) {
     w = (b0 & 0xf) | ((b0 >> 4) << 8) | ((b1 & 0xf) << 16) | ((b1 >> 4) << 24);
 }
 
+// one Q2_0 byte (codes of 4 consecutive elements, 2 bits each) -> 4 int8 c - 2
+__device__ __forceinline__ int unpack_q2_byte(uint32_t x) {
+    const uint32_t spread = (x & 0x3u) | ((x & 0xCu) << 6) | ((x & 0x30u) << 12) | ((x & 0xC0u) << 18);
+    return (int)__vsub4(spread, 0x02020202u);
+}
+
 template <int WT>
 __device__ __forceinline__ void load_w_tile(const uint8_t* __restrict__ qplane,
                                             const __half* __restrict__ dplane,
@@ -37,6 +44,13 @@ __device__ __forceinline__ void load_w_tile(const uint8_t* __restrict__ qplane,
                 uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
                 ws[tid][0] = v0.x; ws[tid][1] = v0.y; ws[tid][2] = v0.z; ws[tid][3] = v0.w;
                 ws[tid][4] = v1.x; ws[tid][5] = v1.y; ws[tid][6] = v1.z; ws[tid][7] = v1.w;
+            } else if (WT == MOE_W_Q2_0) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(qplane + (size_t)j * (k / 4) + b * 8));
+                const uint32_t in[2] = {v.x, v.y};
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) ws[tid][4 * h + t] = unpack_q2_byte((in[h] >> (8 * t)) & 0xffu);
             } else {
                 const uint4* p = reinterpret_cast<const uint4*>(qplane + (size_t)j * (k / 2) + b * 16);
                 uint4 v = __ldg(p);
@@ -183,6 +197,9 @@ int launch_mmq_simt(int wtype, bool gateup, const uint8_t* group_base, size_t sl
     if (wtype == MOE_W_Q8_0) {
         if (gateup) MOE_SIMT_LAUNCH(MOE_W_Q8_0, true);
         else MOE_SIMT_LAUNCH(MOE_W_Q8_0, false);
+    } else if (wtype == MOE_W_Q2_0) {
+        if (gateup) MOE_SIMT_LAUNCH(MOE_W_Q2_0, true);
+        else MOE_SIMT_LAUNCH(MOE_W_Q2_0, false);
     } else {
         if (gateup) MOE_SIMT_LAUNCH(MOE_W_Q4_1, true);
         else MOE_SIMT_LAUNCH(MOE_W_Q4_1, false);

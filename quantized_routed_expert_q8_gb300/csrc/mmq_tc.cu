@@ -80,7 +80,8 @@ __host__ __device__ constexpr int cround(int x, int a) { return (x + a - 1) / a 
 
 template <int WT>
 struct Lay {
-    static constexpr int WROW = WT == MOE_W_Q8_0 ? 128 : 64;  // raw weight bytes per row per stage
+    // raw weight bytes per row per stage (KBS blocks)
+    static constexpr int WROW = WT == MOE_W_Q8_0 ? 128 : WT == MOE_W_Q2_0 ? 32 : 64;
     static constexpr int W_RAW = 2 * BM * WROW;
     static constexpr int X_RAW = BN * 128;
     static constexpr int WS_RAW = 2 * KBS * BM * 2;
@@ -356,6 +357,19 @@ __device__ __forceinline__ void cvt_u4x8(uint32_t w, uint32_t (&h)[4]) {
     h[1] = hsub2_bits(((w >> 4) & 0x000F000Fu) | H1024, H1024);
     h[2] = hsub2_bits(((w >> 8) & 0x000F000Fu) | H1024, H1024);
     h[3] = hsub2_bits(((w >> 12) & 0x000F000Fu) | H1024, H1024);
+}
+
+// 16 2-bit codes c (one word: byte j holds elements 4j..4j+3, element 4j+i in
+// bits 2i..2i+1) -> fp16 pairs of c - 2: a = (e0,e4) (e1,e5) (e2,e6) (e3,e7) and
+// b = (e8,e12) (e9,e13) (e10,e14) (e11,e15), the within-8 order of the 4-bit path
+constexpr uint32_t H1026 = 0x64026402u;  // fp16 (1026, 1026)
+__device__ __forceinline__ void cvt_u2x16(uint32_t w, uint32_t (&a)[4], uint32_t (&b)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t t = (w >> (2 * k)) & 0x03030303u;  // codes of elements k, 4+k, 8+k, 12+k
+        a[k] = hsub2_bits(prmt(t, MAGIC, 0x4140u), H1026);
+        b[k] = hsub2_bits(prmt(t, MAGIC, 0x4342u), H1026);
+    }
 }
 
 // byte offset of (row, 16-byte chunk c) in the fp16 K-major operand layout:
@@ -669,6 +683,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int rep = 0; rep < NW; ++rep) {
                 if (WT == MOE_W_Q8_0) {
                     wv[rep] = *(const uint4*)(st + L::O_W + (rep * 64 + R0) * 128 + ch * 16);
+                } else if (WT == MOE_W_Q2_0) {
+                    // 2-bit rows are 8 bytes a block, unswizzled: thread ct loads row ct
+                    const uint2 v2 = *(const uint2*)(st + L::O_W + (rep * 128 + ct) * 32 + blk * 8);
+                    wv[rep] = make_uint4(v2.x, v2.y, 0u, 0u);
                 } else {
                     const int R = rep * 128 + ct;
                     wv[rep] = *(const uint4*)(st + L::O_W + R * 64 + ((blk ^ ((R >> 1) & 3)) * 16));
@@ -703,6 +721,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint8_t* dst = fa + (R >> 7) * (BM * 64);
                     *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
                     *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
+                } else if (WT == MOE_W_Q2_0) {
+                    const int R = rep * 128 + ct;
+                    const uint32_t w2[2] = {wv[rep].x, wv[rep].y};
+                    uint8_t* dst = fa + (R >> 7) * (BM * 64);
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) {  // elements 16*c2 .. 16*c2 + 15
+                        uint32_t a[4], b[4];
+                        cvt_u2x16(w2[c2], a, b);
+                        *(uint4*)(dst + f16_off(R & 127, 2 * c2)) = make_uint4(a[0], a[1], a[2], a[3]);
+                        *(uint4*)(dst + f16_off(R & 127, 2 * c2 + 1)) = make_uint4(b[0], b[1], b[2], b[3]);
+                    }
                 } else {
                     const int R = rep * 128 + ct;
                     const uint32_t w4[4] = {wv[rep].x, wv[rep].y, wv[rep].z, wv[rep].w};
@@ -935,7 +964,10 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     const MatLayout& ML = GU ? RL.gu : RL.dn;
     const uint8_t* mbase = group_base + (GU ? RL.gate : RL.down);
     const uint64_t S = (uint64_t)E;    // slots addressable in the group buffer
-    const uint64_t wrow = (uint64_t)K / (WT == MOE_W_Q4_1 ? 2 : 1);
+    const uint64_t wrow = (uint64_t)quant_row_bytes(WT, K);
+    const CUtensorMapSwizzle wsw = WT == MOE_W_Q8_0   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : WT == MOE_W_Q4_1 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
     CUtensorMap mW, mWs, mWm, mX, mXs;
     bool ok = true;
     if (GU) {
@@ -943,7 +975,7 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
         uint64_t sq[3] = {wrow, RL.gu.bytes, slot_stride};
         uint32_t bq[4] = {(uint32_t)L::WROW, BM, 2, 1};
         ok &= make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, mbase + ML.q, dq, sq, bq,
-                       WT == MOE_W_Q8_0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "W (gate/up)");
+                       wsw, "W (gate/up)");
         uint64_t ds[4] = {(uint64_t)rows, (uint64_t)(K / QK), 2, S};
         uint64_t ss[3] = {(uint64_t)rows * 2, RL.gu.bytes, slot_stride};
         uint32_t bs[4] = {BM, KBS, 2, 1};
@@ -957,7 +989,7 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
         uint64_t sq[2] = {wrow, slot_stride};
         uint32_t bq[3] = {(uint32_t)L::WROW, 2 * BM, 1};
         ok &= make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, mbase + ML.q, dq, sq, bq,
-                       WT == MOE_W_Q8_0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "W (down)");
+                       wsw, "W (down)");
         uint64_t ds[3] = {(uint64_t)rows, (uint64_t)(K / QK), S};
         uint64_t ss[2] = {(uint64_t)rows * 2, slot_stride};
         uint32_t bs[3] = {2 * BM, KBS, 1};
@@ -1011,11 +1043,13 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
 }  // namespace tc
 
 bool mmq_tc_supported(int wtype, bool gateup, int d, int f) {
-    if (wtype != MOE_W_Q8_0 && wtype != MOE_W_Q4_1) return false;
+    if (wtype != MOE_W_Q8_0 && wtype != MOE_W_Q4_1 && wtype != MOE_W_Q2_0) return false;
     if (d % 256 || f % 128) return false;  // whole 128-row weight tiles, 128-wide K stages
     if (tc::encode_fn() == nullptr) return false;
     if (wtype == MOE_W_Q8_0)
         return gateup ? tc::kernel_ready<MOE_W_Q8_0, true>() : tc::kernel_ready<MOE_W_Q8_0, false>();
+    if (wtype == MOE_W_Q2_0)
+        return gateup ? tc::kernel_ready<MOE_W_Q2_0, true>() : tc::kernel_ready<MOE_W_Q2_0, false>();
     return gateup ? tc::kernel_ready<MOE_W_Q4_1, true>() : tc::kernel_ready<MOE_W_Q4_1, false>();
 }
 
@@ -1029,6 +1063,11 @@ int launch_mmq_tc(int wtype, bool gateup, const uint8_t* group_base, size_t slot
         return gateup ? tc::launch<MOE_W_Q8_0, true>(group_base, slot_stride, E, xq, xds, R, d, f,
                                                      out, ws, W, stream)
                       : tc::launch<MOE_W_Q8_0, false>(group_base, slot_stride, E, xq, xds, R, d, f,
+                                                      out, ws, W, stream);
+    if (wtype == MOE_W_Q2_0)
+        return gateup ? tc::launch<MOE_W_Q2_0, true>(group_base, slot_stride, E, xq, xds, R, d, f,
+                                                     out, ws, W, stream)
+                      : tc::launch<MOE_W_Q2_0, false>(group_base, slot_stride, E, xq, xds, R, d, f,
                                                       out, ws, W, stream);
     return gateup ? tc::launch<MOE_W_Q4_1, true>(group_base, slot_stride, E, xq, xds, R, d, f, out,
                                                  ws, W, stream)

@@ -263,7 +263,8 @@ def test_mmq_down(name):
 
 
 @pytest.mark.parametrize("stage", ["gateup", "down"])
-@pytest.mark.parametrize("name", [mw.TINY.name, mw.T600.name, mw.T2048.name, mw.T8192.name])
+@pytest.mark.parametrize("name", [mw.TINY.name, mw.T600.name, mw.T2048.name, mw.T8192.name,
+                                  mw.T2048_Q2.name])
 def test_mmq_tensor_cores_match_cuda_cores(name, stage, monkeypatch):
     """The tcgen05 kernel forms each block's integer dot exactly and scales it in
     the same fp32 order as the dp4a kernel, so the two agree bit for bit."""
