@@ -65,8 +65,8 @@ constexpr int THREADS = 512;
 // (setmaxnreg.inc), so both the CTA's total and every sub-partition's share
 // stay as launched.
 constexpr int LAUNCH_REGS = 128;  // 65536 / 512
-constexpr int EPI_REGS = 224;
-constexpr int CVT_REGS = 40;
+constexpr int EPI_REGS = 216;
+constexpr int CVT_REGS = 56;
 constexpr int AUX_REGS = 24;
 static_assert(2 * EPI_REGS + CVT_REGS + AUX_REGS == 4 * LAUNCH_REGS, "register split must balance");
 static_assert(THREADS * LAUNCH_REGS <= 65536, "launch registers exceed the register file");
