@@ -448,6 +448,10 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_ab:
         # after the timed region: these calls reuse the layer's buffers
         line["ab"] = ab_compare(m, layer, x, ids, flush, K)
+        try:  # the fused calls take the tensor-core shapes only
+            line["fused"] = fused_compare(m, layer, x, ids, w, flush)
+        except m.MoeError as e:
+            line["fused"] = {"unavailable": str(e)}
     if args.streamed:
         line["streamed"] = streamed_measure(m, layer, wl, x, ids, w, flush, args, ms, n_active)
     if world == 1 and not args.no_cpu_baseline:
@@ -490,6 +494,67 @@ def streamed_measure(m, layer, wl, x, ids, w, flush, args, resident_ms, n_active
             "ring_groups": args.ring_groups, "h2d_bytes_per_step": int(h2d),
             "h2d_GB/s_over_step": round(h2d / t / 1e6, 1),
             "vs_resident_ms": round(t / resident_ms, 3)}
+
+
+def fused_compare(m, layer, x, ids, w, flush, reps: int = 10):
+    """The fused epilogues against the seven calls: the whole layer each way,
+    and each fused call against the two calls it replaces; outputs compared
+    byte for byte."""
+    import torch
+
+    L = layer
+    T, K = ids.shape
+    R, E, d, f = T * K, L.E, L.d, L.f
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        tot = 0.0
+        for i in range(reps):
+            flush.fill_(i & 0xFF)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / reps
+
+    t_layer = timed(lambda: L.forward(x, ids, w))
+    ref = L.out[:T].clone()
+    hq_ref, y_ref = L.hq.clone(), L.y.clone()
+    t_layer_f = timed(lambda: L.forward(x, ids, w, fused=True))
+    same = bool(torch.equal(L.out[:T], ref) and torch.equal(L.hq, hq_ref)
+                and torch.equal(L.y, y_ref))
+
+    def gu_requant():
+        m.moe_grouped_mmq_gateup(L.wtype, L.group_buf, L.slot_stride, L.active, L.n_active,
+                                 L.offsets, E, L.q, L.ds, R, d, f, L.h, L.ws)
+        m.moe_requant_hidden_q8_1(L.h, R, f, L.hq, L.hds)
+
+    def gu_fused():
+        m.moe_grouped_mmq_gateup_q8_1(L.wtype, L.group_buf, L.slot_stride, L.active, L.n_active,
+                                      L.offsets, E, L.q, L.ds, R, d, f, L.hq, L.hds, L.ws)
+
+    def down_combine():
+        m.moe_grouped_mmq_down(L.wtype, L.group_buf, L.slot_stride, L.active, L.n_active,
+                               L.offsets, E, L.hq, L.hds, R, d, f, L.y, L.ws)
+        m.moe_combine_topk(L.y, R, L.slot, w, T, K, d, L.out)
+
+    def down_fused():
+        m.moe_grouped_mmq_down_combine(L.wtype, L.group_buf, L.slot_stride, L.active, L.n_active,
+                                       L.offsets, E, L.hq, L.hds, R, d, f, L.src, L.slot, w, T, K,
+                                       L.y, L.out, L.ws)
+
+    res = {"layer_ms": round(t_layer, 4), "layer_fused_ms": round(t_layer_f, 4),
+           "gateup_requant_ms": round(timed(gu_requant), 4),
+           "gateup_q8_1_ms": round(timed(gu_fused), 4),
+           "down_combine_ms": round(timed(down_combine), 4),
+           "down_combine_fused_ms": round(timed(down_fused), 4),
+           "bytes_identical": same}
+    assert m.moe_device_error(L.ws) == 0
+    return res
 
 
 def ab_compare(m, layer, x, ids, flush, K, reps: int = 10):

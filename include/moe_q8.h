@@ -10,6 +10,9 @@
  *   5. moe_requant_hidden_q8_1    q8_1 re-quantization of the hidden rows
  *   6. moe_grouped_mmq_down       down projection
  *   7. moe_combine_topk           weighted sum of each token's K rows
+ * and two fused forms (the same results, fewer passes over HBM):
+ *   4+5. moe_grouped_mmq_gateup_q8_1   stage 4 writing stage 5's q8_1 rows
+ *   6+7. moe_grouped_mmq_down_combine  stage 6 with stage 7 in its epilogue
  *
  * Sources (pull-request pages of the "Strata" engine):
  *   [#1368] "prefill: quantize each token's MoE input once and scatter it to its
@@ -190,6 +193,24 @@ int moe_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* 
                             void* stream);
 
 /*
+ * Stages 4 and 5 in one launch: the gate/up product of stage 4 whose epilogue
+ * quantizes the hidden rows to q8_1 itself (stage 5, [#1368] intro, applied to
+ * h) instead of writing h.  hq int8 [R][f] and hds uint16 [R][f/32][2] out are
+ * byte-identical to moe_grouped_mmq_gateup followed by moe_requant_hidden_q8_1
+ * (same fp32 h, same block arithmetic).  The pages name a fused expert path
+ * ([#439] rebase note, [#1368] "Identity" tests) without defining it; this is
+ * our own fusion.  Tensor-core kernel only: returns MOE_ERR_UNSUPPORTED where
+ * moe_grouped_mmq_gateup would take the CUDA-core kernel (d % 256 != 0,
+ * f % 128 != 0, or MOE_MMQ_PATH=simt).  hds 4-byte aligned; otherwise as
+ * stage 4.
+ */
+int moe_grouped_mmq_gateup_q8_1(int wtype, const uint8_t* group_base, size_t slot_stride,
+                                const int32_t* active, const int32_t* n_active,
+                                const int32_t* offsets, int E, const int8_t* q, const uint16_t* ds,
+                                int R, int d, int f, int8_t* hq, uint16_t* hds, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/*
  * Stage 6 -- grouped quantized matmul, down projection: y[r,i] = sum over
  * blocks b of dWd[i,b]*dh[r,b]*I_b (+ mWd[i,b]*sh[r,b] for Q4_1), fp32.
  *   hq, hds from stage 5; y float [R][d] out.  Alignment as stage 4.
@@ -209,6 +230,27 @@ int moe_grouped_mmq_down(int wtype, const uint8_t* group_base, size_t slot_strid
  */
 int moe_combine_topk(const float* y, int R, const int32_t* slot, const float* w, int T, int K,
                      int d, float* out, void* stream);
+
+/*
+ * Stages 6 and 7 in one call: the down product of stage 6 (y float [R][d] is
+ * written as there) with the combine of stage 7 done in its epilogue.  Each
+ * row of a work item counts down its token's arrival counter for the item's
+ * 256 output columns (a workspace region, set by a small kernel first); the
+ * item that writes a token's last row computes out[t, those columns] with
+ * stage 7's arithmetic (fma chain over k ascending from 0), so out is
+ * bit-identical to moe_grouped_mmq_down followed by moe_combine_topk whatever
+ * the order in which items finish.  A token with no valid row gets a zero row.
+ *   src [R] and slot [T*K] from stage 1; w float [T*K]; out float [T][d] out,
+ *   16-byte aligned; R must equal T*K.  The workspace is the one
+ *   moe_workspace_size(T, K, E, d, f) sizes.  Tensor-core kernel only, as the
+ *   gate/up fusion (MOE_ERR_UNSUPPORTED otherwise); otherwise as stage 6.
+ */
+int moe_grouped_mmq_down_combine(int wtype, const uint8_t* group_base, size_t slot_stride,
+                                 const int32_t* active, const int32_t* n_active,
+                                 const int32_t* offsets, int E, const int8_t* hq,
+                                 const uint16_t* hds, int R, int d, int f, const int32_t* src,
+                                 const int32_t* slot, const float* w, int T, int K, float* y,
+                                 float* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Stage 1 without a workspace.  The pull-request pages have no counterpart of

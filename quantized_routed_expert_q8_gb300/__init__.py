@@ -50,6 +50,10 @@ _SIGNATURES = {
     "moe_requant_hidden_q8_1": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_grouped_mmq_down": (_I, [_I, _P, _Z, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_combine_topk": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_grouped_mmq_gateup_q8_1": (_I, [_I, _P, _Z, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P,
+                                         _P, _Z, _P]),
+    "moe_grouped_mmq_down_combine": (_I, [_I, _P, _Z, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P,
+                                          _P, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_build_slot_map_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_layer_forward_streamed": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _Z, _Z,
                                         _I, _P, _P, _P]),
@@ -200,6 +204,26 @@ def moe_combine_topk(y, R, slot, w, T, K, d, out, stream=None):
            "moe_combine_topk")
 
 
+def moe_grouped_mmq_gateup_q8_1(wtype, group_base, slot_stride, active, n_active, offsets, E, q,
+                                ds, R, d, f, hq, hds, ws, stream=None):
+    _dev(group_base, active, n_active, offsets, q, ds, hq, hds, ws)
+    _check(lib().moe_grouped_mmq_gateup_q8_1(wtype, _p(group_base), slot_stride, _p(active),
+                                             _p(n_active), _p(offsets), E, _p(q), _p(ds), R, d, f,
+                                             _p(hq), _p(hds), _p(ws),
+                                             ws.numel() * ws.element_size(), _s(stream)),
+           "moe_grouped_mmq_gateup_q8_1")
+
+
+def moe_grouped_mmq_down_combine(wtype, group_base, slot_stride, active, n_active, offsets, E, hq,
+                                 hds, R, d, f, src, slot, w, T, K, y, out, ws, stream=None):
+    _dev(group_base, active, n_active, offsets, hq, hds, src, slot, w, y, out, ws)
+    _check(lib().moe_grouped_mmq_down_combine(wtype, _p(group_base), slot_stride, _p(active),
+                                              _p(n_active), _p(offsets), E, _p(hq), _p(hds), R, d,
+                                              f, _p(src), _p(slot), _p(w), T, K, _p(y), _p(out),
+                                              _p(ws), ws.numel() * ws.element_size(), _s(stream)),
+           "moe_grouped_mmq_down_combine")
+
+
 def moe_build_slot_map_noalloc(ids, E, offsets, slot, src, active, n_active, stream=None):
     """moe_build_slot_map without a workspace, for callers that cannot allocate
     device memory: the scratch is a fixed device array inside the library (see
@@ -282,9 +306,10 @@ class MoeLayer:
         self.ws = torch.zeros((ws_bytes + 255) // 256 * 256, dtype=torch.uint8, device=device)
         moe_workspace_init(self.ws)
 
-    def forward(self, x, ids, w, stream=None):
+    def forward(self, x, ids, w, stream=None, fused=False):
         """x f32 [T, d], ids int32 [T, K], w f32 [T, K] on the GPU -> out [T, d]
-        (a view of the layer's output buffer)."""
+        (a view of the layer's output buffer).  fused=True runs stages 4+5 and
+        6+7 as the two fused calls (same bytes; tensor-core shapes only)."""
         T = x.shape[0]
         assert T <= self.T_max and ids.shape == (T, self.K) and w.shape == (T, self.K)
         K, E, d, f = self.K, self.E, self.d, self.f
@@ -294,6 +319,15 @@ class MoeLayer:
         moe_quantize_scatter_q8_1(x, self.slot, K, R, self.q, self.ds, stream)
         moe_group_gather_active(self.arena, self.rec_bytes, self.arena_stride, self.active,
                                 self.n_active, E, self.group_buf, self.slot_stride, stream)
+        if fused:
+            moe_grouped_mmq_gateup_q8_1(self.wtype, self.group_buf, self.slot_stride, self.active,
+                                        self.n_active, self.offsets, E, self.q, self.ds, R, d, f,
+                                        self.hq, self.hds, self.ws, stream)
+            moe_grouped_mmq_down_combine(self.wtype, self.group_buf, self.slot_stride, self.active,
+                                         self.n_active, self.offsets, E, self.hq, self.hds, R, d,
+                                         f, self.src, self.slot, w, T, K, self.y, self.out,
+                                         self.ws, stream)
+            return self.out[:T]
         moe_grouped_mmq_gateup(self.wtype, self.group_buf, self.slot_stride, self.active,
                                self.n_active, self.offsets, E, self.q, self.ds, R, d, f, self.h,
                                self.ws, stream)

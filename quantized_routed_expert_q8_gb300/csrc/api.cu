@@ -26,7 +26,7 @@ int launch_mmq_simt(int, bool, const uint8_t*, size_t, const int32_t*, const int
                     uint8_t*, const WsLayout&, cudaStream_t);
 int launch_mmq_tc(int, bool, const uint8_t*, size_t, const int32_t*, const int32_t*,
                   const int32_t*, int, const int8_t*, const uint16_t*, int, int, int, float*,
-                  uint8_t*, const WsLayout&, cudaStream_t);
+                  uint8_t*, const WsLayout&, const MmqFused&, cudaStream_t);
 bool mmq_tc_supported(int wtype, bool gateup, int d, int f);
 }  // namespace moe
 
@@ -60,26 +60,32 @@ int check_ws(void* ws, size_t ws_bytes, size_t need) {
     return MOE_OK;
 }
 
+// F: the fused epilogues (tensor-core kernel only), or null
 int mmq_common(int wtype, bool gateup, const uint8_t* group_base, size_t slot_stride,
                const int32_t* active, const int32_t* n_active, const int32_t* offsets, int E,
                const int8_t* xq, const uint16_t* xds, int R, int d, int f, float* out, void* ws,
-               size_t ws_bytes, void* stream) {
+               size_t ws_bytes, void* stream, const MmqFused* F = nullptr, size_t ws_need = 0) {
     if (!wtype_ok(wtype) || R < 0 || d <= 0 || f <= 0 || E <= 0 || E > MAX_E)
         return MOE_ERR_INVALID_ARG;
     if (d % QK || f % QK) return MOE_ERR_INVALID_ARG;
     if (!active || !n_active || !offsets) return MOE_ERR_INVALID_ARG;
-    if (R > 0 && (!group_base || !xq || !xds || !out)) return MOE_ERR_INVALID_ARG;
+    const bool q8_out = F && F->hq;
+    if (R > 0 && (!group_base || !xq || !xds || (!out && !q8_out))) return MOE_ERR_INVALID_ARG;
+    if (q8_out && R > 0 && !F->hds) return MOE_ERR_INVALID_ARG;
     if (!al(group_base, 128) || slot_stride % 128) return MOE_ERR_ALIGNMENT;
     if (!al(xq, 16) || !al(xds, 16) || !al(out, 16)) return MOE_ERR_ALIGNMENT;
+    if (q8_out && !al(F->hds, 4)) return MOE_ERR_ALIGNMENT;
     // the tile list needs R/16 + E entries: size it as if T*K = R
     WsLayout W = ws_layout(R, 1, E, d, f);
-    int rc = check_ws(ws, ws_bytes, W.total);
+    int rc = check_ws(ws, ws_bytes, W.core > ws_need ? W.core : ws_need);
     if (rc) return rc;
+    const bool tc = !force_simt() && mmq_tc_supported(wtype, gateup, d, f);
+    if (F && !tc) return MOE_ERR_UNSUPPORTED;
     if (R == 0) return MOE_OK;
     uint8_t* w8 = (uint8_t*)ws;
-    if (!force_simt() && mmq_tc_supported(wtype, gateup, d, f))
+    if (tc)
         return launch_mmq_tc(wtype, gateup, group_base, slot_stride, active, n_active, offsets, E,
-                             xq, xds, R, d, f, out, w8, W, S(stream));
+                             xq, xds, R, d, f, out, w8, W, F ? *F : MmqFused{}, S(stream));
     return launch_mmq_simt(wtype, gateup, group_base, slot_stride, active, n_active, offsets, E, xq,
                            xds, R, d, f, out, w8, W, S(stream));
 }
@@ -174,6 +180,19 @@ int moe_grouped_mmq_gateup(int wtype, const uint8_t* group_base, size_t slot_str
                       d, f, h, ws, ws_bytes, stream);
 }
 
+int moe_grouped_mmq_gateup_q8_1(int wtype, const uint8_t* group_base, size_t slot_stride,
+                                const int32_t* active, const int32_t* n_active,
+                                const int32_t* offsets, int E, const int8_t* q, const uint16_t* ds,
+                                int R, int d, int f, int8_t* hq, uint16_t* hds, void* ws,
+                                size_t ws_bytes, void* stream) {
+    MmqFused F;
+    F.hq = hq;
+    F.hds = hds;
+    if (R > 0 && (!hq || !hds)) return MOE_ERR_INVALID_ARG;
+    return mmq_common(wtype, true, group_base, slot_stride, active, n_active, offsets, E, q, ds, R,
+                      d, f, nullptr, ws, ws_bytes, stream, &F);
+}
+
 int moe_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
                             void* stream) {
     if (R < 0 || f <= 0 || f % QK) return MOE_ERR_INVALID_ARG;
@@ -189,6 +208,36 @@ int moe_grouped_mmq_down(int wtype, const uint8_t* group_base, size_t slot_strid
                          float* y, void* ws, size_t ws_bytes, void* stream) {
     return mmq_common(wtype, false, group_base, slot_stride, active, n_active, offsets, E, hq, hds,
                       R, d, f, y, ws, ws_bytes, stream);
+}
+
+int moe_grouped_mmq_down_combine(int wtype, const uint8_t* group_base, size_t slot_stride,
+                                 const int32_t* active, const int32_t* n_active,
+                                 const int32_t* offsets, int E, const int8_t* hq,
+                                 const uint16_t* hds, int R, int d, int f, const int32_t* src,
+                                 const int32_t* slot, const float* w, int T, int K, float* y,
+                                 float* out, void* ws, size_t ws_bytes, void* stream) {
+    if (T < 0 || K <= 0 || (long long)T * K != R) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!out || !slot || !w || !src)) return MOE_ERR_INVALID_ARG;
+    if (R > 0 && (!group_base || !hq || !hds || !y)) return MOE_ERR_INVALID_ARG;
+    if (d <= 0 || d % 4) return MOE_ERR_INVALID_ARG;
+    if (!al(out, 16)) return MOE_ERR_ALIGNMENT;
+    const WsLayout W = ws_layout(T, K, E, d, f);
+    MmqFused F;
+    F.comb = out;
+    F.src = src;
+    F.slot = slot;
+    F.w = w;
+    F.arrivals = (int32_t*)((uint8_t*)ws + W.arrivals);
+    F.K = K;
+    F.T = T;
+    // argument and workspace checks first, nothing launched on failure
+    int rc = mmq_common(wtype, false, group_base, slot_stride, active, n_active, offsets, E, hq,
+                        hds, 0, d, f, y, ws, ws_bytes, stream, &F, W.total);
+    if (rc != MOE_OK) return rc;
+    rc = launch_combine_arrivals(slot, T, K, R, d, F.arrivals, out, S(stream));
+    if (rc != MOE_OK) return rc;
+    return mmq_common(wtype, false, group_base, slot_stride, active, n_active, offsets, E, hq, hds,
+                      R, d, f, y, ws, ws_bytes, stream, &F, W.total);
 }
 
 int moe_combine_topk(const float* y, int R, const int32_t* slot, const float* w, int T, int K,

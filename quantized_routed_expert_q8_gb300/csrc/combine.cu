@@ -5,6 +5,7 @@
 // One thread per 4 outputs (16-byte loads and stores); a warp reads 512
 // contiguous bytes of each of the token's K rows.
 #include "common.cuh"
+#include "mmq.cuh"
 
 namespace moe {
 
@@ -44,6 +45,34 @@ int launch_combine_topk(const float* y, int R, const int32_t* slot, const float*
     int grid = (int)(blocks < cap ? blocks : cap);
     combine_topk_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(y), R, slot, w,
                                                   T, K, d / 4, reinterpret_cast<float4*>(out));
+    count_launches(1);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Before the down projection with the combine: arrivals[t][cb] = the number of
+// valid rows of token t (slot in [0, R)) for every 256-column block cb, and the
+// output row of a token with no valid row is zero (no item will combine it).
+__global__ void __launch_bounds__(256) combine_arrivals_kernel(const int32_t* __restrict__ slot,
+                                                               int T, int K, int R, int ncb,
+                                                               int d4, int32_t* __restrict__ arrivals,
+                                                               float4* __restrict__ out) {
+    const int stride = gridDim.x * blockDim.x;
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += stride) {
+        int need = 0;
+        for (int k = 0; k < K; ++k) need += (unsigned)__ldg(slot + (size_t)t * K + k) < (unsigned)R;
+        for (int cb = 0; cb < ncb; ++cb) arrivals[(size_t)t * ncb + cb] = need;
+        if (need == 0)
+            for (int c = 0; c < d4; ++c) out[(size_t)t * d4 + c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+int launch_combine_arrivals(const int32_t* slot, int T, int K, int R, int d, int32_t* arrivals,
+                            float* out, cudaStream_t stream) {
+    if (T == 0) return MOE_OK;
+    int blocks = (T + 255) / 256;
+    if (blocks > 1024) blocks = 1024;
+    combine_arrivals_kernel<<<blocks, 256, 0, stream>>>(slot, T, K, R, (d + 255) / 256, d / 4,
+                                                        arrivals, reinterpret_cast<float4*>(out));
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -57,7 +57,9 @@ __host__ __device__ inline RecLayout rec_layout(int wtype, int d, int f) {
 }
 
 // Workspace: [header 256 B: error word, counters][slot-map chunk counts]
-//            [tile list][spare]
+//            [tile list][spare 256 B][combine arrival counters]
+// The slot-map and MMQ calls use everything before the arrival counters
+// (`core` bytes); the down projection with the combine uses them too.
 constexpr int SLOT_CHUNK = 1024;  // (t,k) entries per slot-map chunk
 constexpr int MAX_E = 8192;
 
@@ -66,13 +68,14 @@ struct WsLayout {
     size_t counters;      // uint32 counters[48]
     size_t chunk_counts;  // int32 [n_chunks][E]
     size_t tiles;         // int4 [max_tiles]
+    size_t arrivals;      // int32 [T][ceil(d/256)]
+    size_t core;          // bytes up to the arrival counters
     size_t total;
     int n_chunks;
     int max_tiles;
 };
 
 inline WsLayout ws_layout(int T, int K, int E, int d, int f) {
-    (void)d;
     (void)f;
     WsLayout W;
     long long TK = (long long)T * K;
@@ -84,7 +87,9 @@ inline WsLayout ws_layout(int T, int K, int E, int d, int f) {
     W.tiles = W.chunk_counts + cc;
     // smallest row tile of any MMQ schedule is 16 rows; one partial tile per expert
     W.max_tiles = (int)(TK / 16 + E + 16);
-    W.total = W.tiles + align_up((size_t)W.max_tiles * 16, 256) + 256;
+    W.core = W.tiles + align_up((size_t)W.max_tiles * 16, 256) + 256;
+    W.arrivals = W.core;
+    W.total = W.core + align_up((size_t)(T > 0 ? T : 0) * (size_t)((d + 255) / 256) * 4, 256);
     return W;
 }
 

@@ -11,6 +11,21 @@ enum { MMQ_COUNTER_NTILES = 0, MMQ_COUNTER_TICKET = 1 };
 int launch_mmq_tiles(const int32_t* active, const int32_t* n_active, const int32_t* offsets,
                      int E, int R, int BM, uint8_t* ws, const WsLayout& W, cudaStream_t stream);
 
+// Optional fused epilogues of the tensor-core MMQ; all null: plain h / y rows.
+struct MmqFused {
+    int8_t* hq = nullptr;      // gate/up: q8_1 hidden quants [R][f] written instead of h
+    uint16_t* hds = nullptr;   // gate/up: (d, s) binary16 pairs [R][f/32]
+    float* comb = nullptr;     // down: combined output [T][d], besides y
+    const int32_t* src = nullptr;
+    const int32_t* slot = nullptr;
+    const float* w = nullptr;
+    int32_t* arrivals = nullptr;  // [T][d/256], set by launch_combine_arrivals
+    int K = 0, T = 0;
+};
+
+int launch_combine_arrivals(const int32_t* slot, int T, int K, int R, int d, int32_t* arrivals,
+                            float* out, cudaStream_t stream);
+
 // SiLU(g) * u in fp32 with SiLU(g) = g / (1 + exp(-g)), IEEE division.
 __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);

@@ -97,9 +97,12 @@ struct Lay {
     static constexpr int O_F16 = RS * STAGE;
     static constexpr int O_SC = O_F16 + NFS * F16_SLOT;
     static constexpr int O_BAR = O_SC + NSC * SC_SLOT;
-    static constexpr int N_BARS = 2 * (RS + NFS + NSC + NTB);
+    // full/empty pairs of the four rings, plus the epilogue warps' own barrier
+    static constexpr int N_BARS = 2 * (RS + NFS + NSC + NTB) + 1;
     static constexpr int O_ITEMS = cround(O_BAR + N_BARS * 8 + 16, 16);
-    static constexpr int SMEM = O_ITEMS + ITEM_RING * 16 + 1024;  // + alignment slack
+    // down with the combine: [0] count, [1..BN] tokens whose rows are all written
+    static constexpr int O_LIST = O_ITEMS + ITEM_RING * 16;
+    static constexpr int SMEM = O_LIST + (BN + 1) * 4 + 1024;  // + alignment slack
 };
 
 // ------------------------------------------------------------------ PTX ----
@@ -372,6 +375,52 @@ __device__ __forceinline__ void cvt_u2x16(uint32_t w, uint32_t (&a)[4], uint32_t
     }
 }
 
+// q8_1 of 16 tokens' 32-value blocks, one value of each per lane (the
+// hidden-row re-quantization of "#1368 ...", intro, done in the gate/up
+// epilogue): the stand-alone quantizer's operations, d = amax/127 and
+// q = round-half-away(v/d) with IEEE division, s = d * sum(q), so the bytes are
+// identical.  Token n0 + i is stored if it is below `rows`; lane 0 stores (d, s).
+__device__ __forceinline__ void requant16(const float (&v)[16], int n0, int rows, int8_t* q0,
+                                          int q_stride, __half2* ds0, int ds_stride, int lane) {
+    float amax[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax[i] = fmaxf(0.0f, fabsf(v[i]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax[i] = fmaxf(amax[i], __shfl_xor_sync(0xffffffffu, amax[i], o));
+    float d[16];
+    int qi[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        d[i] = 0.0f;
+        qi[i] = 0;
+        if (amax[i] != 0.0f) {  // warp-uniform
+            d[i] = __fdiv_rn(amax[i], 127.0f);
+            float x = roundf(__fdiv_rn(v[i], d[i]));
+            x = fminf(127.0f, fmaxf(-127.0f, x));
+            qi[i] = (int)x;
+        }
+    }
+    int sum[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sum[i] = qi[i];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], o);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int n = n0 + i;
+        if (n < rows) {
+            q0[(size_t)n * q_stride] = (int8_t)qi[i];
+            if (lane == 0)
+                ds0[(size_t)n * ds_stride] =
+                    __halves2half2(__float2half_rn(d[i]), __float2half_rn(__fmul_rn(d[i], (float)sum[i])));
+        }
+    }
+}
+
 // byte offset of (row, 16-byte chunk c) in the fp16 K-major operand layout:
 // [row/8][chunk 0..3][row%8][16 B]  (lbo = 128, sbo = 512)
 __device__ __forceinline__ uint32_t f16_off(int row, int c) {
@@ -384,8 +433,19 @@ struct Params {
     int mt_count;  // weight-row tiles per token tile
     int nb;        // 32-blocks of the reduction
     int n_out;     // output row length (f for gate/up, d for down)
-    float* out;
+    int R;         // rows
+    float* out;    // fp32 rows [R][n_out] (gate/up: h, unless hq is set; down: y)
     uint32_t* err;
+    // gate/up: q8_1 hidden rows written by the epilogue instead of h
+    int8_t* hq;    // [R][f]
+    __half2* hds;  // [R][f/32] (d, s)
+    // down: the top-k combine of every (token, 256-column block) whose rows are complete
+    float* comb;            // [T][d]
+    const int32_t* src;     // row -> token
+    const int32_t* slot;    // t*K + k -> row
+    const float* wts;       // [T*K] top-k weights
+    int32_t* arrivals;      // [T][d/256] rows of the token still to be written
+    int K, T;
 };
 
 struct Item {
@@ -407,7 +467,7 @@ __device__ __forceinline__ Item load_item(const Params& P, int it) {
     return I;
 }
 
-template <int WT, bool GU>
+template <int WT, bool GU, bool FUSED>
 __global__ void __launch_bounds__(THREADS, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mWs,
                   const __grid_constant__ CUtensorMap mWm, const __grid_constant__ CUtensorMap mX,
@@ -427,6 +487,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int B_F16_FULL = 2 * RS, B_F16_EMPTY = B_F16_FULL + NFS;
     constexpr int B_SC_FULL = B_F16_EMPTY + NFS, B_SC_EMPTY = B_SC_FULL + NSC;
     constexpr int B_TM_FULL = B_SC_EMPTY + NSC, B_TM_EMPTY = B_TM_FULL + NTB;
+    constexpr int B_EPI = B_TM_EMPTY + NTB;  // the epilogue warps meet at an item's end
 
     const int n_items = *P.n_tiles * P.mt_count;
     if ((int)blockIdx.x >= n_items) return;
@@ -454,6 +515,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar(B_TM_FULL + i), 1);
             mbar_init(bar(B_TM_EMPTY + i), EPI_WARPS);
         }
+        mbar_init(bar(B_EPI), EPI_WARPS);
+        *(int*)(smem + L::O_LIST) = 0;
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -540,6 +603,64 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 8; ++j) accA[c][j] = accB[c][j] = 0ull;
         const uint32_t lanes = tmem + ((uint32_t)(q * 32) << 16);
+        // the 8 epilogue warps meet (bounded; false on abort or timeout)
+        int epi_phase = 0;
+        auto epi_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_EPI));
+            const bool ok = wait_warp(bar(B_EPI), epi_phase & 1);
+            ++epi_phase;
+            return ok;
+        };
+        // Down with the top-k combine ("#1282 ...", "What it does"), after the
+        // item's y stores: every row of the item counts down its (token,
+        // 256-column block); the item that writes a token's last row combines it,
+        //   out[t, c] = fma chain over k ascending of w[t*K+k] * y[slot[t*K+k], c],
+        // the stand-alone combine's arithmetic, so the result is the same whichever
+        // item comes last.
+        auto combine_item = [&](const Item& I) -> bool {
+            int* list = (int*)(smem + L::O_LIST);
+            const int et = threadIdx.x;  // 0..255
+            const int ncb = P.n_out / (2 * BM), cb = I.w0 / (2 * BM);
+            __threadfence();  // this thread's y stores, device-wide, before the count
+            if (!epi_sync()) return false;
+            if (et < I.rows) {
+                const int t = P.src[I.r0 + et];  // the row's token
+                if ((unsigned)t < (unsigned)P.T) {
+                    __threadfence();
+                    if (atomicSub(&P.arrivals[(size_t)t * ncb + cb], 1) == 1) {
+                        __threadfence();
+                        list[1 + atomicAdd(&list[0], 1)] = t;
+                    }
+                } else {
+                    set_error(P.err, MOE_DEV_ERR_BAD_ROWS);
+                }
+            }
+            if (!epi_sync()) return false;
+            const int nl = list[0];
+            __threadfence();  // the other items' y rows of these tokens
+            // thread: 16-byte column c4 of every fourth listed token
+            const int c4 = et & 63;
+            for (int li = et >> 6; li < nl; li += EPI_WARPS * 32 / 64) {
+                const int t = list[1 + li];
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < P.K; ++k) {
+                    const int r = P.slot[(size_t)t * P.K + k];
+                    if ((unsigned)r >= (unsigned)P.R) continue;
+                    const float wk = P.wts[(size_t)t * P.K + k];
+                    const float4 v =
+                        __ldcg(reinterpret_cast<const float4*>(P.out + (size_t)r * P.n_out + I.w0) + c4);
+                    acc.x = __fmaf_rn(wk, v.x, acc.x);
+                    acc.y = __fmaf_rn(wk, v.y, acc.y);
+                    acc.z = __fmaf_rn(wk, v.z, acc.z);
+                    acc.w = __fmaf_rn(wk, v.w, acc.w);
+                }
+                reinterpret_cast<float4*>(P.comb + (size_t)t * P.n_out + I.w0)[c4] = acc;
+            }
+            if (!epi_sync()) return false;  // the list is read: it may be reset
+            if (et == 0) list[0] = 0;
+            return true;
+        };
         int i = 0, b = 0;  // item and block within the item of idx
         for (int idx = 0; idx < total; ++idx) {
             const int tb = idx % NTB, ss = idx % NSC;
@@ -609,28 +730,56 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (b == nb - 1) {
                 // item complete: write this thread's row for every valid token
+                if constexpr (GU && FUSED) {
+                    // h as q8_1: the 32 lanes of this warp hold one 32-column block
+                    // of each token; 16 tokens at a time so that their shuffle and
+                    // division chains overlap
+                    const int kb = (I.w0 + q * 32) / QK;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 4; ++c) {
+                        float v[16];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float a[2], bb[2];
-                        upk2(accA[c][j], a[0], a[1]);
-                        upk2(accB[c][j], bb[0], bb[1]);
+                        for (int j = 0; j < 8; ++j) {
+                            float a0, a1, b0, b1;
+                            upk2(accA[c][j], a0, a1);
+                            upk2(accB[c][j], b0, b1);
+                            v[2 * j] = silu_mul(a0, b0);
+                            v[2 * j + 1] = silu_mul(a1, b1);
+                            accA[c][j] = accB[c][j] = 0ull;
+                        }
+                        const int n0 = h * 64 + c * 16;
+                        if (n0 < I.rows)  // warp-uniform
+                            requant16(v, n0, I.rows, P.hq + (size_t)I.r0 * P.n_out + I.w0 + m,
+                                      P.n_out, P.hds + (size_t)I.r0 * (P.n_out / QK) + kb,
+                                      P.n_out / QK, lane);
+                    }
+                } else {
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int n = h * 64 + c * 16 + 2 * j + e;
-                            if (n < I.rows) {
-                                float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
-                                if (GU) {
-                                    o[0] = silu_mul(a[e], bb[e]);
-                                } else {
-                                    o[0] = a[e];
-                                    o[BM] = bb[e];
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            float a[2], bb[2];
+                            upk2(accA[c][j], a[0], a[1]);
+                            upk2(accB[c][j], bb[0], bb[1]);
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int n = h * 64 + c * 16 + 2 * j + e;
+                                if (n < I.rows) {
+                                    float* o = P.out + (size_t)(I.r0 + n) * P.n_out + I.w0 + m;
+                                    if (GU) {
+                                        o[0] = silu_mul(a[e], bb[e]);
+                                    } else {
+                                        o[0] = a[e];
+                                        o[BM] = bb[e];
+                                    }
                                 }
                             }
+                            accA[c][j] = accB[c][j] = 0ull;
                         }
-                        accA[c][j] = accB[c][j] = 0ull;
                     }
+                }
+                if constexpr (!GU && FUSED) {
+                    if (!combine_item(I)) break;
                 }
                 b = 0;
                 ++i;
@@ -925,13 +1074,13 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
 // LAUNCH_REGS registers (setmaxnreg.inc waits until warpgroup 2 has released
 // enough): check the compiled kernel once, with the shared-memory opt-in,
 // before any launch.
-template <int WT, bool GU>
+template <int WT, bool GU, bool FUSED = false>
 bool kernel_ready() {
     static bool ok = false;
     static std::once_flag once;
     std::call_once(once, [] {
         cudaFuncAttributes a;
-        cudaError_t e = cudaFuncGetAttributes(&a, mmq_tc_kernel<WT, GU>);
+        cudaError_t e = cudaFuncGetAttributes(&a, mmq_tc_kernel<WT, GU, FUSED>);
         if (e != cudaSuccess) {
             if (debug()) std::fprintf(stderr, "moe_q8: mmq_tc attributes: %s\n", cudaGetErrorString(e));
             return;
@@ -942,7 +1091,7 @@ bool kernel_ready() {
                              a.numRegs, a.maxThreadsPerBlock, LAUNCH_REGS, THREADS);
             return;
         }
-        e = cudaFuncSetAttribute(mmq_tc_kernel<WT, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(mmq_tc_kernel<WT, GU, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Lay<WT>::SMEM);
         if (e != cudaSuccess) {
             if (debug()) std::fprintf(stderr, "moe_q8: smem attribute failed: %s\n", cudaGetErrorString(e));
@@ -953,10 +1102,10 @@ bool kernel_ready() {
     return ok;
 }
 
-template <int WT, bool GU>
+template <int WT, bool GU, bool FUSED>
 int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* xq,
            const uint16_t* xds, int R, int d, int f, float* out, uint8_t* ws, const WsLayout& W,
-           cudaStream_t stream) {
+           const MmqFused& F, cudaStream_t stream) {
     using L = Lay<WT>;
     const RecLayout RL = rec_layout(WT, d, f);
     const int K = GU ? d : f;          // reduction
@@ -1013,7 +1162,7 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     }
     if (!ok) return MOE_ERR_CUDA;
 
-    if (!kernel_ready<WT, GU>()) return MOE_ERR_UNSUPPORTED;
+    if (!kernel_ready<WT, GU, FUSED>()) return MOE_ERR_UNSUPPORTED;
     static int sms = 0;
     static std::once_flag sms_once;
     std::call_once(sms_once, [] {
@@ -1027,11 +1176,21 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     P.mt_count = GU ? f / BM : d / (2 * BM);
     P.nb = K / QK;
     P.n_out = GU ? f : d;
+    P.R = R;
     P.out = out;
     P.err = (uint32_t*)(ws + W.err);
+    P.hq = GU ? F.hq : nullptr;
+    P.hds = GU ? reinterpret_cast<__half2*>(F.hds) : nullptr;
+    P.comb = GU ? nullptr : F.comb;
+    P.src = F.src;
+    P.slot = F.slot;
+    P.wts = F.w;
+    P.arrivals = F.arrivals;
+    P.K = F.K;
+    P.T = F.T;
     long long upper = ((long long)R / BN + E + 1) * P.mt_count;
     int grid = (int)(upper < sms ? upper : sms);
-    mmq_tc_kernel<WT, GU><<<grid, THREADS, L::SMEM, stream>>>(mW, mWs, mWm, mX, mXs, P);
+    mmq_tc_kernel<WT, GU, FUSED><<<grid, THREADS, L::SMEM, stream>>>(mW, mWs, mWm, mX, mXs, P);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess && debug())
@@ -1053,26 +1212,38 @@ bool mmq_tc_supported(int wtype, bool gateup, int d, int f) {
     return gateup ? tc::kernel_ready<MOE_W_Q4_1, true>() : tc::kernel_ready<MOE_W_Q4_1, false>();
 }
 
+namespace tc {
+template <int WT>
+int launch_wt(bool gateup, const uint8_t* group_base, size_t slot_stride, int E, const int8_t* xq,
+              const uint16_t* xds, int R, int d, int f, float* out, uint8_t* ws,
+              const WsLayout& W, const MmqFused& F, cudaStream_t stream) {
+    const bool fused = gateup ? F.hq != nullptr : F.comb != nullptr;
+    if (gateup)
+        return fused ? launch<WT, true, true>(group_base, slot_stride, E, xq, xds, R, d, f, out, ws,
+                                              W, F, stream)
+                     : launch<WT, true, false>(group_base, slot_stride, E, xq, xds, R, d, f, out,
+                                               ws, W, F, stream);
+    return fused ? launch<WT, false, true>(group_base, slot_stride, E, xq, xds, R, d, f, out, ws, W,
+                                           F, stream)
+                 : launch<WT, false, false>(group_base, slot_stride, E, xq, xds, R, d, f, out, ws,
+                                            W, F, stream);
+}
+}  // namespace tc
+
 int launch_mmq_tc(int wtype, bool gateup, const uint8_t* group_base, size_t slot_stride,
                   const int32_t* active, const int32_t* n_active, const int32_t* offsets, int E,
                   const int8_t* xq, const uint16_t* xds, int R, int d, int f, float* out,
-                  uint8_t* ws, const WsLayout& W, cudaStream_t stream) {
+                  uint8_t* ws, const WsLayout& W, const MmqFused& F, cudaStream_t stream) {
     int rc = launch_mmq_tiles(active, n_active, offsets, E, R, tc::BN, ws, W, stream);
     if (rc != MOE_OK) return rc;
     if (wtype == MOE_W_Q8_0)
-        return gateup ? tc::launch<MOE_W_Q8_0, true>(group_base, slot_stride, E, xq, xds, R, d, f,
-                                                     out, ws, W, stream)
-                      : tc::launch<MOE_W_Q8_0, false>(group_base, slot_stride, E, xq, xds, R, d, f,
-                                                      out, ws, W, stream);
+        return tc::launch_wt<MOE_W_Q8_0>(gateup, group_base, slot_stride, E, xq, xds, R, d, f, out,
+                                         ws, W, F, stream);
     if (wtype == MOE_W_Q2_0)
-        return gateup ? tc::launch<MOE_W_Q2_0, true>(group_base, slot_stride, E, xq, xds, R, d, f,
-                                                     out, ws, W, stream)
-                      : tc::launch<MOE_W_Q2_0, false>(group_base, slot_stride, E, xq, xds, R, d, f,
-                                                      out, ws, W, stream);
-    return gateup ? tc::launch<MOE_W_Q4_1, true>(group_base, slot_stride, E, xq, xds, R, d, f, out,
-                                                 ws, W, stream)
-                  : tc::launch<MOE_W_Q4_1, false>(group_base, slot_stride, E, xq, xds, R, d, f, out,
-                                                  ws, W, stream);
+        return tc::launch_wt<MOE_W_Q2_0>(gateup, group_base, slot_stride, E, xq, xds, R, d, f, out,
+                                         ws, W, F, stream);
+    return tc::launch_wt<MOE_W_Q4_1>(gateup, group_base, slot_stride, E, xq, xds, R, d, f, out, ws,
+                                     W, F, stream);
 }
 
 }  // namespace moe
