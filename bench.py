@@ -220,10 +220,10 @@ def alu_partials(cfg, R: int) -> float:
 PROFILED_TRAFFIC = {
     ("mmq_gateup", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/mmq_tc.cu",
-        "sha256_16": "b20871039c8af3d3", "bytes": 610223104 + 254831104},
+        "sha256_16": "df9c507d8623531a", "bytes": 610050816 + 254977792},
     ("mmq_down", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/mmq_tc.cu",
-        "sha256_16": "b20871039c8af3d3", "bytes": 279392256 + 666368000},
+        "sha256_16": "df9c507d8623531a", "bytes": 279342336 + 665958912},
     ("quantize_scatter", "T32768_d2048_f768_E512_K10_q4_1"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/quantize.cu",
         "sha256_16": "90d587e478e32e24", "bytes": 269889792 + 694902272},
