@@ -76,3 +76,33 @@ def test_host_checks_reject_before_launch(lib):
     assert L.moe_grouped_mmq_gateup(0, P(128), 100, P(16), P(16), P(16), 4, P(16), P(16), 8, 64,
                                     64, P(16), P(256), 1 << 20, None) == -2
     assert L.moe_combine_topk(P(16), 8, P(16), P(16), 2, 2, 6, P(16), None) == -1
+
+
+def test_fused_calls_reject_before_launch(lib):
+    """The fused calls' host checks: R must be T*K, outputs must be present, and
+    the workspace must include the combine's arrival counters."""
+    import quantized_routed_expert_q8_gb300 as m
+    L = m.lib()
+    P = ctypes.c_void_p
+    T, K, E, d, f = 16, 2, 4, 256, 128
+    R = T * K
+    need = m.moe_workspace_size(T, K, E, d, f)
+    core = m.moe_workspace_size(T, K, E, 0, f)
+    assert need - core == (T * ((d + 255) // 256) * 4 + 255) // 256 * 256
+    args = (0, P(128), 128, P(16), P(16), P(16), E, P(16), P(16))
+    # R != T*K, K == 0
+    assert L.moe_grouped_mmq_down_combine(*args, R - 1, d, f, P(16), P(16), P(16), T, K, P(16),
+                                          P(16), P(256), need, None) == -1
+    assert L.moe_grouped_mmq_down_combine(*args, 0, d, f, P(16), P(16), P(16), T, 0, P(16),
+                                          P(16), P(256), need, None) == -1
+    # no output, misaligned output
+    assert L.moe_grouped_mmq_down_combine(*args, R, d, f, P(16), P(16), P(16), T, K, P(16),
+                                          None, P(256), need, None) == -1
+    assert L.moe_grouped_mmq_down_combine(*args, R, d, f, P(16), P(16), P(16), T, K, P(16),
+                                          P(20), P(256), need, None) == -2
+    # a workspace sized without the arrival counters
+    assert L.moe_grouped_mmq_down_combine(*args, R, d, f, P(16), P(16), P(16), T, K, P(16),
+                                          P(16), P(256), core, None) == -3
+    # gate/up to q8_1 without its outputs, or with misaligned (d, s) pairs
+    assert L.moe_grouped_mmq_gateup_q8_1(*args, R, d, f, None, P(16), P(256), need, None) == -1
+    assert L.moe_grouped_mmq_gateup_q8_1(*args, R, d, f, P(16), P(18), P(256), need, None) == -2
