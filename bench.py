@@ -216,31 +216,41 @@ def alu_partials(cfg, R: int) -> float:
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a
 # stage's main kernel, from one ncu capture (summaries under profiles/), valid
-# only while the kernel source is the one that was profiled.
+# only while the kernel's code is the code that was profiled: "code_sha256_16"
+# hashes the source with its comments and blank lines removed (code_digest), so
+# a comment edit keeps the figure and any code change drops it.
 PROFILED_TRAFFIC = {
     ("mmq_gateup", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/mmq_tc.cu",
-        "sha256_16": "df9c507d8623531a", "bytes": 610050816 + 254977792},
+        "code_sha256_16": "abc4fd640fc3ab6c", "bytes": 610050816 + 254977792},
     ("mmq_down", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/mmq_tc.cu",
-        "sha256_16": "df9c507d8623531a", "bytes": 279342336 + 665958912},
+        "code_sha256_16": "abc4fd640fc3ab6c", "bytes": 279342336 + 665958912},
     ("quantize_scatter", "T32768_d2048_f768_E512_K10_q4_1"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/quantize.cu",
-        "sha256_16": "90d587e478e32e24", "bytes": 269889792 + 694902272},
+        "code_sha256_16": "50f7d37a16a0671c", "bytes": 269889792 + 694902272},
 }
 
 
-def profiled_traffic(stage: str, workload: str):
+def code_digest(text: str) -> str:
+    """sha256 prefix of C/CUDA source without comments and blank lines."""
     import hashlib
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
+def profiled_traffic(stage: str, workload: str):
     rec = PROFILED_TRAFFIC.get((stage, workload))
     if not rec:
         return None
-    path = os.path.join(ROOT, rec["source"])
     try:
-        digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+        digest = code_digest(open(os.path.join(ROOT, rec["source"])).read())
     except OSError:
         return None
-    return rec["bytes"] if rec["sha256_16"] == digest else None
+    return rec["bytes"] if rec["code_sha256_16"] == digest else None
 
 
 # ------------------------------------------------------------ multi-rank --

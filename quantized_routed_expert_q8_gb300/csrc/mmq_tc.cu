@@ -29,6 +29,10 @@
 //     (128 fp32 per thread) and writes the item's outputs.
 // setmaxnreg moves registers from the converter/producer warpgroups to the
 // epilogue warpgroups.
+// The FUSED instantiations change only an item's end: gate/up writes its hidden
+// rows as q8_1 (the stand-alone re-quantization's bytes) instead of fp32, and
+// down, after its y rows, counts each row's token down and combines the tokens
+// whose last row it wrote (the stand-alone combine's bytes).
 // Every wait is bounded: on timeout the kernel sets MOE_DEV_ERR_TIMEOUT, drains
 // what it started and exits.
 #include <cudaTypedefs.h>
