@@ -685,6 +685,8 @@ def run_stage(args):
     L = m.MoeLayer(cfg.wtype, E, d, f, K, T, arena, wl.rec_bytes, st, dev)
     L.forward(x, ids, w)
     calls = {
+        "slot_map": lambda: m.moe_build_slot_map(ids, E, L.offsets, L.slot, L.src, L.active,
+                                                 L.n_active, L.ws),
         "quantize_scatter": lambda: m.moe_quantize_scatter_q8_1(x, L.slot, K, R, L.q, L.ds),
         "group_gather": lambda: m.moe_group_gather_active(L.arena, L.rec_bytes, L.arena_stride,
                                                           L.active, L.n_active, E, L.group_buf,
@@ -809,7 +811,7 @@ def main():
     ap.add_argument("--no-ab", action="store_true",
                     help="skip the gather-quantization and per-expert gather comparisons")
     ap.add_argument("--stage", default=None,
-                    help="time one stage alone (for profiler captures): quantize_scatter, "
+                    help="time one stage alone (for profiler captures): slot_map, quantize_scatter, "
                          "mmq_gateup, mmq_down, requant_hidden, combine_topk, group_gather")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -124,8 +124,10 @@ int moe_build_slot_map(const int32_t* ids, int T, int K, int E, int32_t* offsets
  * write the blocks to all K of its rows slot[t*K+k] (the same bytes as the
  * per-row gather quantizer).
  *   x    float [T][d], 16-byte aligned.    slot int32 [T*K].
- *   q    int8 [R][d] out, 8-byte aligned.  ds uint16 [R][d/32][2] out, 4-byte aligned.
- * Rows with slot outside [0, R) are skipped.  d % 32 == 0.
+ *   q    int8 [R][d] out, 16-byte aligned.  ds uint16 [R][d/32][2] out, 4-byte aligned.
+ * Rows with slot outside [0, R) are skipped.  d % 32 == 0.  A block whose
+ * d = amax/127 is zero in fp32 (amax == 0, or amax <= 63 * 2^-149) is stored
+ * as all-zero: x/d is undefined there.
  */
 int moe_quantize_scatter_q8_1(const float* x, int T, int d, int K, const int32_t* slot, int R,
                               int8_t* q, uint16_t* ds, void* stream);
@@ -188,6 +190,7 @@ int moe_grouped_mmq_gateup(int wtype, const uint8_t* group_base, size_t slot_str
  * Stage 5 -- the down-projection q8_1 quantization of the hidden rows ([#1368]
  * intro calls it unchanged): hq int8 [R][f], hds uint16 [R][f/32][2] from
  * h float [R][f].  Same quantizer as stage 2 with the identity row map.
+ * h 16-byte aligned, hq 16-byte aligned, hds 4-byte aligned.
  */
 int moe_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
                             void* stream);

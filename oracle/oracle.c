@@ -210,8 +210,9 @@ int oracle_build_slot_map(const int32_t* ids, int T, int K, int E, int32_t* offs
 
 /* ------------------------------------------------------------------------- */
 /* Stage a2/a5 quantizer: one 32-wide q8_1 block.                             */
-/*   amax = max |v_i| (fp32); if amax == 0 then q = 0, d = 0, s = 0;          */
-/*   else d = amax / 127 (IEEE), q_i = round-half-away(v_i / d) (IEEE),       */
+/*   amax = max |v_i| (fp32); d = amax / 127 (IEEE); if d == 0 (amax == 0,    */
+/*   or amax <= 63 * 2^-149 so that the quotient underflows) then q = 0,       */
+/*   d = 0, s = 0; else q_i = round-half-away(v_i / d) (IEEE),                 */
 /*   S = sum q_i exactly, stored d_h = fp16(d), s_h = fp16(d * S).            */
 /* ------------------------------------------------------------------------- */
 void oracle_quantize_block_q8_1(const float* v, int8_t* q, uint16_t* dh, uint16_t* sh) {
@@ -220,13 +221,13 @@ void oracle_quantize_block_q8_1(const float* v, int8_t* q, uint16_t* dh, uint16_
         float a = fabsf(v[i]);
         if (a > amax) amax = a;
     }
-    if (amax == 0.0f) {
+    float d = amax / 127.0f;
+    if (d == 0.0f) {  /* x / d is undefined: the block is stored as all-zero */
         for (int i = 0; i < QK; ++i) q[i] = 0;
         *dh = 0;
         *sh = 0;
         return;
     }
-    float d = amax / 127.0f;
     int sum = 0;
     for (int i = 0; i < QK; ++i) {
         float r = roundf(v[i] / d);

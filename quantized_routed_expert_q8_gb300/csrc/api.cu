@@ -136,7 +136,7 @@ int moe_quantize_scatter_q8_1(const float* x, int T, int d, int K, const int32_t
     if (T < 0 || K < 0 || R < 0 || d <= 0 || d % QK) return MOE_ERR_INVALID_ARG;
     if ((long long)T * K > 0 && (!x || !slot)) return MOE_ERR_INVALID_ARG;
     if (R > 0 && (!q || !ds)) return MOE_ERR_INVALID_ARG;
-    if (!al(x, 16) || !al(q, 8) || !al(ds, 4)) return MOE_ERR_ALIGNMENT;
+    if (!al(x, 16) || !al(q, 16) || !al(ds, 4)) return MOE_ERR_ALIGNMENT;
     if (T == 0 || K == 0 || R == 0) return MOE_OK;
     return launch_quantize_scatter(x, T, d, K, slot, R, q, ds, S(stream));
 }
@@ -145,7 +145,7 @@ int moe_quantize_gather_q8_1(const float* x, int T, int d, const int32_t* src, i
                              uint16_t* ds, void* stream) {
     if (T < 0 || R < 0 || d <= 0 || d % QK) return MOE_ERR_INVALID_ARG;
     if (R > 0 && (!x || !src || !q || !ds)) return MOE_ERR_INVALID_ARG;
-    if (!al(x, 16) || !al(q, 8) || !al(ds, 4)) return MOE_ERR_ALIGNMENT;
+    if (!al(x, 16) || !al(q, 16) || !al(ds, 4)) return MOE_ERR_ALIGNMENT;
     if (R == 0) return MOE_OK;
     return launch_quantize_gather(x, T, d, src, R, q, ds, S(stream));
 }
@@ -197,7 +197,7 @@ int moe_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* 
                             void* stream) {
     if (R < 0 || f <= 0 || f % QK) return MOE_ERR_INVALID_ARG;
     if (R > 0 && (!h || !hq || !hds)) return MOE_ERR_INVALID_ARG;
-    if (!al(h, 16) || !al(hq, 8) || !al(hds, 4)) return MOE_ERR_ALIGNMENT;
+    if (!al(h, 16) || !al(hq, 16) || !al(hds, 4)) return MOE_ERR_ALIGNMENT;
     if (R == 0) return MOE_OK;
     return launch_requant_hidden(h, R, f, hq, hds, S(stream));
 }

@@ -397,10 +397,9 @@ __device__ __forceinline__ void requant16(const float (&v)[16], int n0, int rows
     int qi[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        d[i] = 0.0f;
+        d[i] = __fdiv_rn(amax[i], 127.0f);
         qi[i] = 0;
-        if (amax[i] != 0.0f) {  // warp-uniform
-            d[i] = __fdiv_rn(amax[i], 127.0f);
+        if (d[i] != 0.0f) {  // warp-uniform; a zero d stores an all-zero block
             float x = roundf(__fdiv_rn(v[i], d[i]));
             x = fminf(127.0f, fmaxf(-127.0f, x));
             qi[i] = (int)x;

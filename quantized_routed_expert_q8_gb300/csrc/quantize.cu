@@ -7,100 +7,113 @@
 // map) share the block arithmetic.
 //
 // q8_1 block: d = amax/127, q = round-half-away(x/d), s = d*sum(q); d and s
-// stored as binary16.  All divisions are IEEE (__fdiv_rn), the product s is a
+// stored as binary16; a block whose d is zero is stored as all-zero.  All divisions are IEEE (__fdiv_rn), the product s is a
 // single rounding (__fmul_rn), and nothing is flushed to zero, so the bytes
 // match any correct implementation of the definition.
 //
-// Mapping: one thread per 8 consecutive values (two 16-byte loads), four
-// threads per 32-block, amax and sum(q) reduced with two xor shuffles.  A warp
-// covers 256 consecutive values of a row: its q stores are 256 contiguous bytes
-// per destination row and its (d, s) stores 32 contiguous bytes.
+// Mapping: one thread per 16 consecutive values (four 16-byte loads), two
+// threads per 32-block, amax and sum(q) reduced with one xor shuffle each.  A
+// warp covers 512 consecutive values of a row: each thread stores its 16 quants
+// as one 16-byte store, so a warp's q stores are 512 contiguous bytes per
+// destination row and its (d, s) stores 64 contiguous bytes.
 #include "common.cuh"
 
 namespace moe {
 
 enum QuantMode { QUANT_SCATTER = 0, QUANT_GATHER = 1, QUANT_IDENTITY = 2 };
 
-struct Q8Block8 {
-    uint2 q;      // 8 int8 quants
-    __half2 ds;   // (d, s), valid in every lane of the 4-lane group
+struct Q8Half {
+    uint4 q;      // 16 int8 quants
+    __half2 ds;   // (d, s), valid in both lanes of the pair
 };
 
-__device__ __forceinline__ Q8Block8 quantize8(const float4 a, const float4 b) {
-    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+__device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[4 * i] = a[i].x;
+        v[4 * i + 1] = a[i].y;
+        v[4 * i + 2] = a[i].z;
+        v[4 * i + 3] = a[i].w;
+    }
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    Q8Block8 r;
+    Q8Half r;
     int sum = 0;
-    uint32_t lo = 0, hi = 0;
-    float d = 0.0f;
-    if (amax != 0.0f) {
-        d = __fdiv_rn(amax, 127.0f);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    // d == 0 (amax == 0, or an fp32-subnormal amax <= 63 * 2^-149 whose quotient
+    // underflows) leaves x / d undefined: such a block is stored as all-zero
+    const float d = __fdiv_rn(amax, 127.0f);
+    if (d != 0.0f) {
+        // q = round-half-away(fp32(v / d)).  With a normal d, qa = v * RN(1/d) is
+        // within 3 ulp of the IEEE quotient, and |qa| < 128 puts an ulp at
+        // <= 2^-17; so unless qa lies within 2^-14 of a half-integer, rounding qa
+        // gives the same integer as rounding the quotient.  Otherwise (and for
+        // a subnormal d) the quotient itself is formed with an IEEE division.
+        const bool fast_ok = d >= 1.17549435e-38f;
+        const float r = fast_ok ? __frcp_rn(d) : 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float x = roundf(__fdiv_rn(v[i], d));
+        for (int i = 0; i < 16; ++i) {
+            const float qa = __fmul_rn(v[i], r);
+            const float fr = fabsf(qa) - truncf(fabsf(qa));
+            float x = roundf(qa);
+            if (!fast_ok || fabsf(fr - 0.5f) <= 6.103515625e-05f) x = roundf(__fdiv_rn(v[i], d));
             x = fminf(127.0f, fmaxf(-127.0f, x));
-            int qi = (int)x;
+            const int qi = (int)x;
             sum += qi;
-            uint32_t byte = (uint32_t)(qi & 0xff);
-            if (i < 4) lo |= byte << (8 * i);
-            else hi |= byte << (8 * (i - 4));
+            w[i >> 2] |= (uint32_t)(qi & 0xff) << (8 * (i & 3));
         }
     }
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    float s = __fmul_rn(d, (float)sum);
-    r.q = make_uint2(lo, hi);
+    const float s = __fmul_rn(d, (float)sum);
+    r.q = make_uint4(w[0], w[1], w[2], w[3]);
     r.ds = __halves2half2(__float2half_rn(d), __float2half_rn(s));
     return r;
 }
 
 // x: [n_src_rows][d]; writes rows of q [R][d] / ds [R][d/32].
 template <int MODE>
-__global__ void __launch_bounds__(256) quantize_q8_1_kernel(
+__global__ void __launch_bounds__(256, 5) quantize_q8_1_kernel(
     const float* __restrict__ x, int n_src_rows, int d, int K, const int32_t* __restrict__ map,
     int R, int8_t* __restrict__ q, __half2* __restrict__ ds, long long n_units) {
-    const int upr = d / 8;  // units (of 8 values) per row
+    const int upr = d / 16;  // units (of 16 values) per row
     const long long stride = (long long)gridDim.x * blockDim.x;
     // round the bound up to a whole warp so every shuffle has all 32 lanes
     const long long bound = (n_units + 31) / 32 * 32;
     for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < bound; u += stride) {
         bool in = u < n_units;
-        long long row = in ? u / upr : 0;
-        int c = in ? (int)(u % upr) * 8 : 0;
+        const long long row = in ? u / upr : 0;
+        const int c = in ? (int)(u % upr) * 16 : 0;
         long long srow = row;  // the x row this unit reads
         if (MODE == QUANT_GATHER) {
-            int t = in ? map[row] : -1;
+            const int t = in ? map[row] : -1;
             in = in && (unsigned)t < (unsigned)n_src_rows;
             srow = in ? t : 0;
         }
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        float4 a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (in) {
             const float4* p = reinterpret_cast<const float4*>(x + srow * d + c);
-            if (MODE == QUANT_GATHER) {  // rows are re-read K times: keep them cached
-                a = __ldg(p);
-                b = __ldg(p + 1);
-            } else {  // read once: stream past L2
-                a = __ldcs(p);
-                b = __ldcs(p + 1);
-            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)  // gather rows are re-read K times: keep them cached;
+                a[i] = MODE == QUANT_GATHER ? __ldg(p + i) : __ldcs(p + i);  // else stream past L2
         }
-        Q8Block8 blk = quantize8(a, b);
+        const Q8Half blk = quantize16(a);
         if (!in) continue;
-        bool lead = (threadIdx.x & 3) == 0;
+        const bool lead = (threadIdx.x & 1) == 0;
         if (MODE == QUANT_SCATTER) {
             for (int k = 0; k < K; ++k) {
-                int r = map[row * K + k];
+                const int r = map[row * K + k];
                 if ((unsigned)r >= (unsigned)R) continue;
-                *reinterpret_cast<uint2*>(q + (size_t)r * d + c) = blk.q;
+                *reinterpret_cast<uint4*>(q + (size_t)r * d + c) = blk.q;
                 if (lead) ds[(size_t)r * (d / QK) + c / QK] = blk.ds;
             }
         } else {
             if (row >= R) continue;
-            *reinterpret_cast<uint2*>(q + (size_t)row * d + c) = blk.q;
+            *reinterpret_cast<uint4*>(q + (size_t)row * d + c) = blk.q;
             if (lead) ds[(size_t)row * (d / QK) + c / QK] = blk.ds;
         }
     }
@@ -111,13 +124,13 @@ static int quant_grid(long long n_units) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     long long blocks = (n_units + 255) / 256;
-    long long cap = (long long)sms * 8;  // 8 resident blocks of 256 per SM
+    long long cap = (long long)sms * 5;  // 5 resident blocks of 256 per SM (48 registers)
     return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
 int launch_quantize_scatter(const float* x, int T, int d, int K, const int32_t* slot, int R,
                             int8_t* q, uint16_t* ds, cudaStream_t stream) {
-    long long n = (long long)T * (d / 8);
+    long long n = (long long)T * (d / 16);
     if (n == 0) return MOE_OK;
     quantize_q8_1_kernel<QUANT_SCATTER><<<quant_grid(n), 256, 0, stream>>>(
         x, T, d, K, slot, R, q, reinterpret_cast<__half2*>(ds), n);
@@ -127,7 +140,7 @@ int launch_quantize_scatter(const float* x, int T, int d, int K, const int32_t* 
 
 int launch_quantize_gather(const float* x, int T, int d, const int32_t* src, int R, int8_t* q,
                            uint16_t* ds, cudaStream_t stream) {
-    long long n = (long long)R * (d / 8);
+    long long n = (long long)R * (d / 16);
     if (n == 0) return MOE_OK;
     quantize_q8_1_kernel<QUANT_GATHER><<<quant_grid(n), 256, 0, stream>>>(
         x, T, d, 1, src, R, q, reinterpret_cast<__half2*>(ds), n);
@@ -137,7 +150,7 @@ int launch_quantize_gather(const float* x, int T, int d, const int32_t* src, int
 
 int launch_requant_hidden(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
                           cudaStream_t stream) {
-    long long n = (long long)R * (f / 8);
+    long long n = (long long)R * (f / 16);
     if (n == 0) return MOE_OK;
     quantize_q8_1_kernel<QUANT_IDENTITY><<<quant_grid(n), 256, 0, stream>>>(
         h, R, f, 1, nullptr, R, hq, reinterpret_cast<__half2*>(hds), n);

@@ -66,3 +66,23 @@ def rel_l2_rows(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
     num = np.linalg.norm((got.astype(np.float64) - ref.astype(np.float64)), axis=-1)
     den = np.linalg.norm(ref.astype(np.float64), axis=-1)
     return np.where(den > 0, num / np.where(den > 0, den, 1), num)
+
+
+def layer_tokens(cfg) -> np.ndarray:
+    """Tokens the layer tests check against the oracle: all of a small workload;
+    for a large one 40 seeded tokens, up to four all-zero tokens and the first
+    and last token."""
+    if cfg.T <= 600:
+        return np.arange(cfg.T)
+    rng = np.random.default_rng(cfg.seed)
+    return np.unique(np.concatenate([rng.integers(0, cfg.T, 40), cfg.zero_list()[:4],
+                                     [0, cfg.T - 1]])).astype(np.int64)
+
+
+def oracle_layer_tokens(wl: mw.Workload, toks) -> np.ndarray:
+    """The oracle's layer output for the listed tokens (each token depends only
+    on its own K rows, so the oracle runs on that token subset)."""
+    cfg = wl.cfg
+    sub = wl.subset(toks)
+    return oracle.layer_forward(cfg.wtype, wl.arena, wl.rec_bytes, wl.arena_stride, sub.x,
+                                sub.ids, sub.w, cfg.E, cfg.d, cfg.f)["out"]

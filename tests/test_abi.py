@@ -59,11 +59,38 @@ def test_status_strings(lib):
     assert m.moe_workspace_size(8192, 10, 512, 2048, 768) > 0
 
 
+class _Buffers:
+    """Pointers for the rejection tests.  With a GPU present every pointer is a
+    real device allocation of 1 MiB (offset by `off` bytes for the misaligned
+    cases), so that a host check that stopped rejecting would launch on valid
+    memory instead of a made-up address; without a GPU nothing can launch and
+    plain aligned integers stand in."""
+
+    def __init__(self):
+        self.keep = []
+        try:
+            import torch
+            self.cuda = torch.cuda.is_available()
+        except ImportError:
+            self.cuda = False
+
+    def __call__(self, off=0):
+        if not self.cuda:
+            return ctypes.c_void_p(4096 * (len(self.keep) + 1) + off)
+        import torch
+        t = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+        self.keep.append(t)
+        return ctypes.c_void_p(t.data_ptr() + off)
+
+
 def test_host_checks_reject_before_launch(lib):
-    """Host-visible misuse returns an error status without touching the GPU."""
+    """Host-visible misuse returns an error status before launching anything."""
     import quantized_routed_expert_q8_gb300 as m
     L = m.lib()
-    P = ctypes.c_void_p
+    B = _Buffers()
+
+    def P(v):  # v = the alignment the old fake address had; v % 16 == 1 means misaligned
+        return B(off=v % 16 if v % 16 else 0)
     # null stream is fine: nothing launches on these paths
     assert L.moe_group_gather(P(16), 16, 16, P(16), 17, 0, P(16), 16, None) == -1
     assert L.moe_group_gather(P(16), 16, 16, P(16), 2, 15, P(16), 16, None) == -1
@@ -83,7 +110,10 @@ def test_fused_calls_reject_before_launch(lib):
     the workspace must include the combine's arrival counters."""
     import quantized_routed_expert_q8_gb300 as m
     L = m.lib()
-    P = ctypes.c_void_p
+    B = _Buffers()
+
+    def P(v):  # misaligned by v % 16 bytes when v is not a multiple of 16
+        return B(off=v % 16)
     T, K, E, d, f = 16, 2, 4, 256, 128
     R = T * K
     need = m.moe_workspace_size(T, K, E, d, f)

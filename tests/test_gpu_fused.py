@@ -6,11 +6,17 @@ moe_grouped_mmq_down_combine the same y rows and the same combined output as
 the down product followed by the stand-alone combine, bit for bit: the fused
 epilogues run the same arithmetic, and the combine's fixed k order does not
 depend on which work item finishes a token last.
+
+Both fused calls are also checked against the oracle itself: the fused layer's
+output (the combine written by moe_grouped_mmq_down_combine) within 2e-3
+relative L2 per token on every workload, all-zero tokens exactly zero, and the
+down + combine call alone on the oracle's own hidden rows.
 """
 import numpy as np
 import pytest
 
 import moe_workloads as mw
+import oracle
 from tests import helpers as H
 
 pytestmark = pytest.mark.gpu
@@ -125,3 +131,60 @@ def test_fused_rejects_what_it_cannot_take():
                                        layer.hq, layer.hds, T * K - 1, layer.d, layer.f,
                                        layer.src, layer.slot, w, T, K, layer.y, layer.out,
                                        layer.ws)
+
+
+@pytest.mark.parametrize("name", [c.name for c in mw.CONFIG_LIST])
+def test_fused_layer_matches_oracle(name):
+    """MoeLayer.forward(fused=True) -- gate/up writing q8_1 hidden rows, then
+    down with the in-kernel combine -- against the oracle's layer: <= 2e-3
+    relative L2 per token (the tolerance of the layer output), zero tokens
+    exactly zero."""
+    wl = H.workload(name)
+    cfg = wl.cfg
+    layer = m.MoeLayer(cfg.wtype, cfg.E, cfg.d, cfg.f, cfg.K, cfg.T, H.to_dev(wl.arena),
+                       wl.rec_bytes, wl.arena_stride)
+    layer.out.fill_(float("nan"))
+    out = layer.forward(H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w), fused=True)
+    out = out.cpu().numpy()
+    assert m.moe_device_error(layer.ws) == 0
+    assert np.isfinite(out).all()
+    toks = H.layer_tokens(cfg)
+    err = H.rel_l2_rows(out[toks], H.oracle_layer_tokens(wl, toks))
+    assert err.max() <= 2e-3, (err.max(), toks[np.argmax(err)])
+    for t in cfg.zero_list():
+        assert not out[t].any()
+
+
+@pytest.mark.parametrize("name", [mw.TINY.name, mw.T600.name, mw.T2048.name, mw.T2048_Q2.name])
+def test_down_combine_matches_oracle(name):
+    """moe_grouped_mmq_down_combine alone, on hidden rows quantized by the
+    oracle: its combined output against the oracle's down product followed by
+    the oracle's combine, within 1e-5 relative L2 per token (the stage-level
+    bar of the down product; the combine adds K fp32 roundings)."""
+    wl = H.workload(name)
+    cfg = wl.cfg
+    T, K, d, f = cfg.T, cfg.K, cfg.d, cfg.f
+    o = oracle.build_slot_map(wl.ids, cfg.E)
+    R = int(o["offsets"][cfg.E])
+    assert R == T * K
+    hid = mw.normal_f32(cfg.seed, 9, R * f, scale=0.05).reshape(R, f)
+    hid[::53] = 0.0
+    hq, hds = oracle.requant_hidden_q8_1(hid)
+    layer = m.MoeLayer(cfg.wtype, cfg.E, d, f, K, T, H.to_dev(wl.arena), wl.rec_bytes,
+                       wl.arena_stride)
+    layer.forward(H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w))  # slot map, group buffers
+    w = H.to_dev(wl.w)
+    layer.out.fill_(float("nan"))
+    m.moe_grouped_mmq_down_combine(layer.wtype, layer.group_buf, layer.slot_stride, layer.active,
+                                   layer.n_active, layer.offsets, layer.E, H.to_dev(hq),
+                                   H.to_dev(hds.view(np.int16)), R, d, f, layer.src, layer.slot, w,
+                                   T, K, layer.y, layer.out)
+    out = layer.out[:T].cpu().numpy()
+    assert m.moe_device_error(layer.ws) == 0
+    toks = H.layer_tokens(cfg)
+    rows = o["slot"].reshape(T, K)[toks].reshape(-1)
+    y_rows = H.oracle_rows("down", wl, o["offsets"], hq, hds, rows)
+    n = len(toks)  # the oracle's combine on the selected tokens' rows, renumbered
+    ref = oracle.combine_topk(y_rows, np.arange(n * K, dtype=np.int32), wl.w[toks], n, K, d)
+    err = H.rel_l2_rows(out[toks], ref)
+    assert err.max() <= 1e-5, (err.max(), toks[np.argmax(err)])

@@ -328,15 +328,8 @@ def test_layer_end_to_end(name):
     out = layer.forward(H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w)).cpu().numpy()
     assert m.moe_device_error(layer.ws) == 0
     assert np.isfinite(out).all()
-    if cfg.T <= 600:
-        toks = np.arange(cfg.T)
-    else:
-        rng = np.random.default_rng(cfg.seed)
-        toks = np.unique(np.concatenate([rng.integers(0, cfg.T, 40), cfg.zero_list()[:4],
-                                         [0, cfg.T - 1]])).astype(np.int64)
-    sub = wl.subset(toks)
-    ref = oracle.layer_forward(cfg.wtype, wl.arena, wl.rec_bytes, wl.arena_stride, sub.x, sub.ids,
-                               sub.w, cfg.E, cfg.d, cfg.f)["out"]
+    toks = H.layer_tokens(cfg)
+    ref = H.oracle_layer_tokens(wl, toks)
     err = H.rel_l2_rows(out[toks], ref)
     assert err.max() <= 2e-3, (err.max(), toks[np.argmax(err)])
     for t in cfg.zero_list():

@@ -79,7 +79,15 @@ def test_noalloc_matches_workspace_form_twice():
 def test_noalloc_rejects_sizes_beyond_its_array():
     L = m.lib()
     P = ctypes.c_void_p
-    # 600 chunks of 1024 entries x 512 experts exceed the 1 MiB count table
-    rc = L.moe_build_slot_map_noalloc(P(256), 61440, 10, 512, P(256), P(256), P(256), P(256),
-                                      P(256), None)
+    # 600 chunks of 1024 entries x 512 experts exceed the 1 MiB count table.  The
+    # buffers are real allocations of the declared shape, so a size check that
+    # stopped rejecting would not launch on made-up addresses.
+    T, K, E = 61440, 10, 512
+    ids = torch.zeros((T, K), dtype=torch.int32, device="cuda")
+    o = _outputs(T, K, E)
+    rc = L.moe_build_slot_map_noalloc(P(ids.data_ptr()), T, K, E, P(o["offsets"].data_ptr()),
+                                      P(o["slot"].data_ptr()), P(o["src"].data_ptr()),
+                                      P(o["active"].data_ptr()), P(o["n_active"].data_ptr()), None)
     assert rc == -4  # MOE_ERR_UNSUPPORTED, before any launch
+    torch.cuda.synchronize()
+    assert int(o["n_active"].item()) == -9  # nothing was written
