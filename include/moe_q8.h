@@ -85,6 +85,8 @@ typedef enum { MOE_W_Q8_0 = 0, MOE_W_Q4_1 = 1, MOE_W_Q2_0 = 2 } moe_wtype;
 #define MOE_DEV_ERR_BAD_EXPERT_ID 0x1u /* an id outside [0, E): its slot is -1 */
 #define MOE_DEV_ERR_BAD_ROWS 0x2u      /* offsets or slot beyond R: rows skipped */
 #define MOE_DEV_ERR_TIMEOUT 0x4u       /* a bounded wait inside a kernel gave up */
+#define MOE_DEV_ERR_RANGE 0x8u         /* a q8_1 or weight block with |d*q| >= 65520: the
+                                          tensor-core MMQ's binary16 operands overflow */
 
 /* Bytes of one expert record (gate, up, down) for the given weight type. */
 size_t moe_expert_record_bytes(int wtype, int d, int f);

@@ -29,6 +29,7 @@ QK = 32
 DEV_ERR_BAD_EXPERT_ID = 0x1
 DEV_ERR_BAD_ROWS = 0x2
 DEV_ERR_TIMEOUT = 0x4
+DEV_ERR_RANGE = 0x8
 
 _lock = threading.Lock()
 _lib = None

@@ -45,11 +45,21 @@ inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline bool al(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline bool wtype_ok(int w) { return w == MOE_W_Q8_0 || w == MOE_W_Q4_1 || w == MOE_W_Q2_0; }
 
-// MOE_MMQ_PATH=simt forces the CUDA-core MMQ (cross-check of the tensor-core path)
-inline bool force_simt() {
+// Kernel choice for the grouped MMQ.  Stage 4 (gate/up) runs on the tensor-core
+// kernel that forms each block's integer dot exactly and scales it on the CUDA
+// cores in the scalar definition's order, so the hidden rows -- which stage 5
+// re-quantizes -- equal the definition's values.  Stage 6 (down) runs on the
+// folded-scale kernel (binary16 hi + lo operands, whole reduction in TMEM), whose
+// result differs from that order by a few fp32 ulps; its output is only
+// combined, never re-quantized.
+// MOE_MMQ_PATH=simt forces the CUDA-core MMQ (the cross-check of the tensor-core
+// paths); =blockscale the per-block-scaling tensor-core kernel for both stages;
+// =fold the folded-scale kernel for both stages.
+inline bool mmq_path_is(const char* name) {
     const char* v = std::getenv("MOE_MMQ_PATH");
-    return v && std::strcmp(v, "simt") == 0;
+    return v && std::strcmp(v, name) == 0;
 }
+inline bool force_simt() { return mmq_path_is("simt"); }
 
 // recover the (T, K) the workspace was sized for is not possible; the MMQ and
 // slot-map calls size it from their own arguments
@@ -81,8 +91,13 @@ int mmq_common(int wtype, bool gateup, const uint8_t* group_base, size_t slot_st
     if (rc) return rc;
     const bool tc = !force_simt() && mmq_tc_supported(wtype, gateup, d, f);
     if (F && !tc) return MOE_ERR_UNSUPPORTED;
+    const bool fold = !F && !force_simt() && !mmq_path_is("blockscale") &&
+                      (!gateup || mmq_path_is("fold")) && mmq_fold_supported(wtype, d, f);
     if (R == 0) return MOE_OK;
     uint8_t* w8 = (uint8_t*)ws;
+    if (fold)
+        return launch_mmq_fold(wtype, gateup, group_base, slot_stride, active, n_active, offsets,
+                               E, xq, xds, R, d, f, out, w8, W, S(stream));
     if (tc)
         return launch_mmq_tc(wtype, gateup, group_base, slot_stride, active, n_active, offsets, E,
                              xq, xds, R, d, f, out, w8, W, F ? *F : MmqFused{}, S(stream));

@@ -23,6 +23,14 @@ struct MmqFused {
     int K = 0, T = 0;
 };
 
+// The grouped MMQ with the block scales folded into binary16 hi + lo operands
+// (stages 4 and 6 on the tensor cores; shapes with d % 256 == 0, f % 128 == 0).
+bool mmq_fold_supported(int wtype, int d, int f);
+int launch_mmq_fold(int wtype, bool gateup, const uint8_t* group_base, size_t slot_stride,
+                    const int32_t* active, const int32_t* n_active, const int32_t* offsets, int E,
+                    const int8_t* xq, const uint16_t* xds, int R, int d, int f, float* out,
+                    uint8_t* ws, const WsLayout& W, cudaStream_t stream);
+
 int launch_combine_arrivals(const int32_t* slot, int T, int K, int R, int d, int32_t* arrivals,
                             float* out, cudaStream_t stream);
 

@@ -15,6 +15,7 @@ __global__ void __launch_bounds__(1024) mmq_tiles_kernel(const int32_t* __restri
                                                          int E, int R, int BM,
                                                          int4* __restrict__ tiles,
                                                          int32_t* __restrict__ n_tiles,
+                                                         int32_t* __restrict__ ticket,
                                                          int max_tiles, uint32_t* err) {
     __shared__ int s_full, s_bad;
     __shared__ int part_hist[256];  // partial tiles by row count (BM <= 256)
@@ -53,6 +54,7 @@ __global__ void __launch_bounds__(1024) mmq_tiles_kernel(const int32_t* __restri
         }
         if (s_bad) set_error(err, MOE_DEV_ERR_BAD_ROWS);
         *n_tiles = min(run, max_tiles);
+        *ticket = 0;  // the persistent MMQ kernels take work items from here
         s_full = 0;  // reused as the full-tile cursor
     }
     __syncthreads();
@@ -78,9 +80,10 @@ int launch_mmq_tiles(const int32_t* active, const int32_t* n_active, const int32
                      int E, int R, int BM, uint8_t* ws, const WsLayout& W, cudaStream_t stream) {
     uint32_t* err = (uint32_t*)(ws + W.err);
     int32_t* n_tiles = (int32_t*)(ws + W.counters) + MMQ_COUNTER_NTILES;
+    int32_t* ticket = (int32_t*)(ws + W.counters) + MMQ_COUNTER_TICKET;
     int4* tiles = (int4*)(ws + W.tiles);
     mmq_tiles_kernel<<<1, 1024, 0, stream>>>(active, n_active, offsets, E, R, BM, tiles, n_tiles,
-                                             W.max_tiles, err);
+                                             ticket, W.max_tiles, err);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

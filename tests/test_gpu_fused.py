@@ -12,6 +12,8 @@ output (the combine written by moe_grouped_mmq_down_combine) within 2e-3
 relative L2 per token on every workload, all-zero tokens exactly zero, and the
 down + combine call alone on the oracle's own hidden rows.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -29,13 +31,24 @@ import quantized_routed_expert_q8_gb300 as m  # noqa: E402
 
 
 def _both(layer, x, ids, w):
-    """(unfused, fused) copies of hq, hds, y and out for one input."""
+    """(unfused, fused) copies of hq, hds, y and out for one input.  The unfused
+    layer runs the per-block-scaling tensor-core kernel for both projections
+    (MOE_MMQ_PATH=blockscale), the kernel the fused epilogues extend."""
     res = []
     for fused in (False, True):
         for t in (layer.hq, layer.hds, layer.y, layer.out):
             t.zero_()
-        out = layer.forward(x, ids, w, fused=fused)
-        torch.cuda.synchronize()
+        old = os.environ.get("MOE_MMQ_PATH")
+        if not fused:
+            os.environ["MOE_MMQ_PATH"] = "blockscale"
+        try:
+            out = layer.forward(x, ids, w, fused=fused)
+            torch.cuda.synchronize()
+        finally:
+            if old is None:
+                os.environ.pop("MOE_MMQ_PATH", None)
+            else:
+                os.environ["MOE_MMQ_PATH"] = old
         res.append({"hq": layer.hq.clone(), "hds": layer.hds.clone(), "y": layer.y.clone(),
                     "out": out.clone(), "err": m.moe_device_error(layer.ws)})
     return res
@@ -178,7 +191,7 @@ def test_down_combine_matches_oracle(name):
     m.moe_grouped_mmq_down_combine(layer.wtype, layer.group_buf, layer.slot_stride, layer.active,
                                    layer.n_active, layer.offsets, layer.E, H.to_dev(hq),
                                    H.to_dev(hds.view(np.int16)), R, d, f, layer.src, layer.slot, w,
-                                   T, K, layer.y, layer.out)
+                                   T, K, layer.y, layer.out, layer.ws)
     out = layer.out[:T].cpu().numpy()
     assert m.moe_device_error(layer.ws) == 0
     toks = H.layer_tokens(cfg)

@@ -246,61 +246,12 @@ def test_group_gather_equals_one_copy_per_expert(rec, arena_off):
             # and against plain slicing
             for j, e in enumerate(ids):
                 s = (first + j) * slot_stride
-                assert np.array_equal(a[s:s + rec], arena[e * stride:e * stride + rec])
+                assert np.array_equal(a[s:s + rec], arena[int(e) * stride:int(e) * stride + rec])
 
 
 # --------------------------------------------------------------------- MMQ ---
 
-def _qbytes(wtype, rows, k):
-    return rows * k // {mw.Q8_0: 1, mw.Q4_1: 2, mw.Q2_0: 4}[wtype]
-
-
-def _planes(wtype, rec, off, rows, k):
-    """Decode one matrix of a record with numpy (independent of the oracle).
-    Q2_0 codes come back as their values c - 2."""
-    qb = _qbytes(wtype, rows, k)
-    a128 = lambda v: (v + 127) // 128 * 128
-    sb = rows * (k // 32) * 2
-    base = rec[off:]
-    if wtype == mw.Q8_0:
-        q = base[:qb].view(np.int8).reshape(rows, k).astype(np.int64)
-    elif wtype == mw.Q2_0:
-        p = base[:qb].reshape(rows, k // 4).astype(np.int64)
-        q = np.empty((rows, k), np.int64)
-        for i in range(4):  # element 4j+i sits in bits 2i..2i+1 of byte j
-            q[:, i::4] = ((p >> (2 * i)) & 3) - 2
-    else:
-        p = base[:qb].reshape(rows, k // 2)
-        q = np.empty((rows, k), np.int64)
-        q[:, 0::2] = p & 0x0F
-        q[:, 1::2] = p >> 4
-    # scale planes are block-major [k/32][rows]
-    dpl = base[a128(qb):a128(qb) + sb].view(np.float16).reshape(k // 32, rows).T.astype(np.float64)
-    mpl = None
-    if wtype == mw.Q4_1:
-        o = a128(qb) + a128(sb)
-        mpl = base[o:o + sb].view(np.float16).reshape(k // 32, rows).T.astype(np.float64)
-    return q, dpl, mpl
-
-
-def _dequant_w(q, dpl, mpl):
-    w = q.astype(np.float64) * np.repeat(dpl, 32, axis=1)
-    if mpl is not None:
-        w += np.repeat(mpl, 32, axis=1)
-    return w
-
-
-def _dequant_x(q, ds):
-    dx = ds[..., 0].view(np.float16).astype(np.float64)
-    return q.astype(np.float64) * np.repeat(dx, 32, axis=1)
-
-
-def _mat_offsets(wtype, d, f):
-    a128 = lambda v: (v + 127) // 128 * 128
-    qb = _qbytes(wtype, f, d)
-    sb = f * (d // 32) * 2
-    g = a128(qb) + a128(sb) * (2 if wtype == mw.Q4_1 else 1)
-    return 0, g, 2 * g
+from tests.helpers import _dequant_w, _dequant_x, _mat_offsets, _planes, _qbytes  # noqa: E402
 
 
 def _silu_mul64(g, u):
@@ -520,7 +471,7 @@ def test_layer_end_to_end_tiny(wtype):
     ref = np.zeros((cfg.T, cfg.d))
     for t in range(cfg.T):
         for k in range(cfg.K):
-            e = wl.ids[t, k]
+            e = int(wl.ids[t, k])
             rec = wl.arena[e * wl.arena_stride:e * wl.arena_stride + wl.rec_bytes]
             G = _dequant_w(*_planes(wtype, rec, og, cfg.f, cfg.d))
             U = _dequant_w(*_planes(wtype, rec, ou, cfg.f, cfg.d))
