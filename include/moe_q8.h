@@ -308,7 +308,9 @@ int moe_build_slot_map_noalloc(const int32_t* ids, int T, int K, int E, int32_t*
  *   - ring: device, ring_groups * 16 * slot_stride bytes; group_buf: device,
  *     16 * slot_stride bytes (128-byte aligned, slot_stride % 128 == 0);
  *     group_counts: device int32 [ceil(E / 16)];
- *     host_scratch: host int32 [2 * E + 2].
+ *     host_scratch: pinned host int32 [2 * E + 2 + ceil(E / 16)] (routed experts,
+ *     their row offsets, then the per-group expert counts staged for the
+ *     device); the caller must not write it while a call is in flight.
  *   - The other buffers as the stage calls document (q, ds for T*K rows of d;
  *     h, hq, hds for T*K rows of f; y for T*K rows of d; ws of
  *     moe_workspace_size(T, K, E, d, f) bytes).

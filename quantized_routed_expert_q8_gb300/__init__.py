@@ -351,7 +351,8 @@ class MoeLayer:
         if not hasattr(self, "stage_buf"):
             self.stage_buf = torch.zeros(16 * self.slot_stride, dtype=torch.uint8, device=dev)
             self.group_counts = torch.zeros((self.E + 15) // 16, dtype=torch.int32, device=dev)
-            self.host_scratch = torch.zeros(2 * self.E + 2, dtype=torch.int32).pin_memory()
+            n_scratch = 2 * self.E + 2 + (self.E + 15) // 16
+            self.host_scratch = torch.zeros(n_scratch, dtype=torch.int32).pin_memory()
             self.copy_stream = torch.cuda.Stream(device=dev)
         b = StreamBuffers()
         for name, t in (("ring", self.ring), ("group_buf", self.stage_buf),

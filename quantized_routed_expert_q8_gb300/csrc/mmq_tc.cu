@@ -800,34 +800,51 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
 
 // The register split relies on the launch giving every thread exactly
 // LAUNCH_REGS registers (setmaxnreg.inc waits until warpgroup 2 has released
-// enough): check the compiled kernel once, with the shared-memory opt-in,
-// before any launch.
+// enough): check the compiled kernel, and opt it into its shared memory, once
+// per device (the opt-in is a property of the device's context) before any
+// launch there.
+constexpr int kMaxDevices = 64;
+
 template <int WT, bool GU, bool FUSED = false>
 bool kernel_ready() {
-    static bool ok = false;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaFuncAttributes a;
-        cudaError_t e = cudaFuncGetAttributes(&a, mmq_tc_kernel<WT, GU, FUSED>);
-        if (e != cudaSuccess) {
-            if (debug()) std::fprintf(stderr, "moe_q8: mmq_tc attributes: %s\n", cudaGetErrorString(e));
-            return;
-        }
-        if (a.numRegs != LAUNCH_REGS || a.maxThreadsPerBlock < THREADS) {
-            if (debug())
-                std::fprintf(stderr, "moe_q8: mmq_tc built with %d registers / %d threads, want %d / %d\n",
-                             a.numRegs, a.maxThreadsPerBlock, LAUNCH_REGS, THREADS);
-            return;
-        }
-        e = cudaFuncSetAttribute(mmq_tc_kernel<WT, GU, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Lay<WT>::SMEM);
-        if (e != cudaSuccess) {
-            if (debug()) std::fprintf(stderr, "moe_q8: smem attribute failed: %s\n", cudaGetErrorString(e));
-            return;
-        }
-        ok = true;
-    });
-    return ok;
+    static std::mutex mu;
+    static signed char state[kMaxDevices] = {};  // 0 unknown, 1 ready, -1 unusable
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (state[dev] != 0) return state[dev] == 1;
+    state[dev] = -1;
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, mmq_tc_kernel<WT, GU, FUSED>);
+    if (e != cudaSuccess) {
+        if (debug()) std::fprintf(stderr, "moe_q8: mmq_tc attributes: %s\n", cudaGetErrorString(e));
+        return false;
+    }
+    if (a.numRegs != LAUNCH_REGS || a.maxThreadsPerBlock < THREADS) {
+        if (debug())
+            std::fprintf(stderr, "moe_q8: mmq_tc built with %d registers / %d threads, want %d / %d\n",
+                         a.numRegs, a.maxThreadsPerBlock, LAUNCH_REGS, THREADS);
+        return false;
+    }
+    e = cudaFuncSetAttribute(mmq_tc_kernel<WT, GU, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Lay<WT>::SMEM);
+    if (e != cudaSuccess) {
+        if (debug()) std::fprintf(stderr, "moe_q8: smem attribute failed: %s\n", cudaGetErrorString(e));
+        return false;
+    }
+    state[dev] = 1;
+    return true;
+}
+
+// SM count of the current device, looked up once per device
+int device_sms() {
+    static std::mutex mu;
+    static int sms[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (sms[dev] == 0) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    return sms[dev];
 }
 
 template <int WT, bool GU, bool FUSED>
@@ -891,13 +908,8 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     if (!ok) return MOE_ERR_CUDA;
 
     if (!kernel_ready<WT, GU, FUSED>()) return MOE_ERR_UNSUPPORTED;
-    static int sms = 0;
-    static std::once_flag sms_once;
-    std::call_once(sms_once, [] {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    });
+    const int sms = device_sms();
+    if (sms <= 0) return MOE_ERR_CUDA;
     Params P;
     P.tiles = (const int4*)(ws + W.tiles);
     P.n_tiles = (const int32_t*)(ws + W.counters) + MMQ_COUNTER_NTILES;

@@ -18,7 +18,8 @@
 // Only routed experts are streamed, in ascending id order, so no ring entry is
 // ever skipped inside an open group.  The host learns which experts are routed
 // from one device-to-host copy after the routing map (the call's one
-// synchronization).  Every product runs in the same kernels as the resident
+// synchronization: the per-group counts go back from the pinned host scratch
+// without another).  Every product runs in the same kernels as the resident
 // layer on the same bytes, so the output is bit-identical to it.
 #include <mutex>
 #include <vector>
@@ -103,13 +104,14 @@ extern "C" int moe_layer_forward_streamed(int wtype, int T, int K, int E, int d,
     if (n_active < 0 || n_active > E) return MOE_ERR_DEVICE;
     const int n_groups = (n_active + GROUP - 1) / GROUP;
 
-    // per-group expert counts, on the device, for the grouped products
-    std::vector<int32_t> counts(n_groups > 0 ? n_groups : 1);
+    // per-group expert counts, on the device, for the grouped products; staged in
+    // the caller's pinned host_scratch, which no later host write touches before
+    // this copy has run (the next call writes it only after its own
+    // synchronization of compute_stream), so the copy needs no wait
+    int32_t* counts = hs + 2 * E + 2;
     for (int g = 0; g < n_groups; ++g) counts[g] = std::min(GROUP, n_active - g * GROUP);
-    if (n_groups > 0 &&
-        (cudaMemcpyAsync(b->group_counts, counts.data(), sizeof(int32_t) * n_groups,
-                         cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-         cudaStreamSynchronize(cs) != cudaSuccess))  // `counts` is pageable and goes out of scope
+    if (n_groups > 0 && cudaMemcpyAsync(b->group_counts, counts, sizeof(int32_t) * n_groups,
+                                        cudaMemcpyHostToDevice, cs) != cudaSuccess)
         return MOE_ERR_CUDA;
 
     EventPool* ev = nullptr;

@@ -60,7 +60,8 @@ def _guard_layer(layer, g, streamed_ring_groups=None):
                                                           dtype=torch.uint8, device=dev))
         layer.group_counts = g.view("group_counts", torch.empty((layer.E + 15) // 16,
                                                                 dtype=torch.int32, device=dev))
-        layer.host_scratch = torch.zeros(2 * layer.E + 2, dtype=torch.int32).pin_memory()
+        n_scratch = 2 * layer.E + 2 + (layer.E + 15) // 16
+        layer.host_scratch = torch.zeros(n_scratch, dtype=torch.int32).pin_memory()
         layer.copy_stream = torch.cuda.Stream(device=dev)
 
 
