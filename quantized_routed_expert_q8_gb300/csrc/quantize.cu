@@ -54,14 +54,25 @@ __device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
         // a subnormal d) the quotient itself is formed with an IEEE division.
         const bool fast_ok = d >= 1.17549435e-38f;
         const float r = fast_ok ? __frcp_rn(d) : 0.0f;
+        float x[16];
+        uint32_t need = fast_ok ? 0u : 0xFFFFu;  // values whose quotient must be exact
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const float qa = __fmul_rn(v[i], r);
             const float fr = fabsf(qa) - truncf(fabsf(qa));
-            float x = roundf(qa);
-            if (!fast_ok || fabsf(fr - 0.5f) <= 6.103515625e-05f) x = roundf(__fdiv_rn(v[i], d));
-            x = fminf(127.0f, fmaxf(-127.0f, x));
-            const int qi = (int)x;
+            x[i] = roundf(qa);
+            if (fabsf(fr - 0.5f) <= 6.103515625e-05f) need |= 1u << i;
+        }
+        // a warp-uniform branch, so that the divisions run only in the rare
+        // warps that need one
+        if (__any_sync(0xffffffffu, need != 0u)) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if ((need >> i) & 1u) x[i] = roundf(__fdiv_rn(v[i], d));
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int qi = (int)fminf(127.0f, fmaxf(-127.0f, x[i]));
             sum += qi;
             w[i >> 2] |= (uint32_t)(qi & 0xff) << (8 * (i & 3));
         }
@@ -75,7 +86,7 @@ __device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
 
 // x: [n_src_rows][d]; writes rows of q [R][d] / ds [R][d/32].
 template <int MODE>
-__global__ void __launch_bounds__(256, 5) quantize_q8_1_kernel(
+__global__ void __launch_bounds__(256, 4) quantize_q8_1_kernel(
     const float* __restrict__ x, int n_src_rows, int d, int K, const int32_t* __restrict__ map,
     int R, int8_t* __restrict__ q, __half2* __restrict__ ds, long long n_units) {
     const int upr = d / 16;  // units (of 16 values) per row
@@ -124,7 +135,7 @@ static int quant_grid(long long n_units) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     long long blocks = (n_units + 255) / 256;
-    long long cap = (long long)sms * 5;  // 5 resident blocks of 256 per SM (48 registers)
+    long long cap = (long long)sms * 4;  // 4 resident blocks of 256 per SM (64 registers)
     return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
