@@ -187,7 +187,8 @@ def layer_accounting(cfg, n_active: int, rec_bytes: int, R: int):
     block dots (2 per multiply-add of routed rows only).  Also the layer's total
     algorithmic bytes and ops."""
     T, d, f, K = cfg.T, cfg.d, cfg.f, cfg.K
-    q8 = 1.125  # bytes per q8_1 value: int8 plus (d, s) fp16 per 32
+    # bytes per q8_1 value: int8 plus (d, s) fp16 per 32, or (d, s, s_lo, s_hi) (D2S6, Q2_K)
+    q8 = 1.25 if cfg.wtype == mw.Q2_K else 1.125
     w_gu = n_active * rec_bytes * 2.0 / 3.0  # gate and up matrices of the routed experts
     w_dn = n_active * rec_bytes / 3.0
     stages = {
@@ -318,19 +319,20 @@ def run_gpu(args, rank, world, local_rank):
 
     stage_names = ["slot_map", "quantize_scatter", "group_gather", "mmq_gateup",
                    "requant_hidden", "mmq_down", "combine_topk"]
+    q_scatter, q_gather, q_requant = m.quantizers(cfg.wtype)
 
     def step(evs=None):
         L = layer
         calls = [
             lambda: m.moe_build_slot_map(ids, E, L.offsets, L.slot, L.src, L.active, L.n_active,
                                          L.ws),
-            lambda: m.moe_quantize_scatter_q8_1(x, L.slot, K, R, L.q, L.ds),
+            lambda: q_scatter(x, L.slot, K, R, L.q, L.ds),
             lambda: m.moe_group_gather_active(L.arena, L.rec_bytes, L.arena_stride, L.active,
                                               L.n_active, E, L.group_buf, L.slot_stride),
             lambda: m.moe_grouped_mmq_gateup(L.wtype, L.group_buf, L.slot_stride, L.active,
                                              L.n_active, L.offsets, E, L.q, L.ds, R, d, f, L.h,
                                              L.ws),
-            lambda: m.moe_requant_hidden_q8_1(L.h, R, f, L.hq, L.hds),
+            lambda: q_requant(L.h, R, f, L.hq, L.hds),
             lambda: m.moe_grouped_mmq_down(L.wtype, L.group_buf, L.slot_stride, L.active,
                                            L.n_active, L.offsets, E, L.hq, L.hds, R, d, f, L.y,
                                            L.ws),
@@ -622,7 +624,7 @@ def fused_compare(m, layer, x, ids, w, flush, reps: int = 10):
     def gu_requant():
         m.moe_grouped_mmq_gateup(L.wtype, L.group_buf, L.slot_stride, L.active, L.n_active,
                                  L.offsets, E, L.q, L.ds, R, d, f, L.h, L.ws)
-        m.moe_requant_hidden_q8_1(L.h, R, f, L.hq, L.hds)
+        m.quantizers(L.wtype)[2](L.h, R, f, L.hq, L.hds)
 
     def gu_fused():
         m.moe_grouped_mmq_gateup_q8_1(L.wtype, L.group_buf, L.slot_stride, L.active, L.n_active,
@@ -680,8 +682,9 @@ def ab_compare(m, layer, x, ids, flush, K, reps: int = 10):
         return tot / reps
 
     q2, ds2 = torch.empty_like(L.q), torch.empty_like(L.ds)
-    t_scatter = timed(lambda: m.moe_quantize_scatter_q8_1(x, L.slot, K, R, L.q, L.ds))
-    t_gather = timed(lambda: m.moe_quantize_gather_q8_1(x, L.src, R, q2, ds2))
+    q_scatter, q_gather, _ = m.quantizers(L.wtype)
+    t_scatter = timed(lambda: q_scatter(x, L.slot, K, R, L.q, L.ds))
+    t_gather = timed(lambda: q_gather(x, L.src, R, q2, ds2))
     q_same = bool(torch.equal(L.q[:R], q2[:R]) and torch.equal(L.ds[:R], ds2[:R]))
 
     ss = L.slot_stride
@@ -752,8 +755,9 @@ def run_stage(args):
         m.moe_workspace_init(ws)
         m.moe_build_slot_map(ids, E, off, slot, src, act, na, ws)
         q = torch.empty((R, d), dtype=torch.int8, device=dev)
-        ds = torch.empty((R, d // 32, 2), dtype=torch.int16, device=dev)
-        return _time_stage(args, cfg, lambda: m.moe_quantize_scatter_q8_1(x, slot, K, R, q, ds),
+        ds = torch.empty((R, d // 32, m.ds_halves(cfg.wtype)), dtype=torch.int16, device=dev)
+        scatter = m.quantizers(cfg.wtype)[0]
+        return _time_stage(args, cfg, lambda: scatter(x, slot, K, R, q, ds),
                            ws, int(na.item()), 0)
     wl = mw.make_workload(cfg)
     # only the routed experts' records go to the device (ids renumbered to them),
@@ -772,14 +776,14 @@ def run_stage(args):
     calls = {
         "slot_map": lambda: m.moe_build_slot_map(ids, E, L.offsets, L.slot, L.src, L.active,
                                                  L.n_active, L.ws),
-        "quantize_scatter": lambda: m.moe_quantize_scatter_q8_1(x, L.slot, K, R, L.q, L.ds),
+        "quantize_scatter": lambda: m.quantizers(cfg.wtype)[0](x, L.slot, K, R, L.q, L.ds),
         "group_gather": lambda: m.moe_group_gather_active(L.arena, L.rec_bytes, L.arena_stride,
                                                           L.active, L.n_active, E, L.group_buf,
                                                           L.slot_stride),
         "mmq_gateup": lambda: m.moe_grouped_mmq_gateup(L.wtype, L.group_buf, L.slot_stride,
                                                        L.active, L.n_active, L.offsets, E, L.q,
                                                        L.ds, R, d, f, L.h, L.ws),
-        "requant_hidden": lambda: m.moe_requant_hidden_q8_1(L.h, R, f, L.hq, L.hds),
+        "requant_hidden": lambda: m.quantizers(cfg.wtype)[2](L.h, R, f, L.hq, L.hds),
         "mmq_down": lambda: m.moe_grouped_mmq_down(L.wtype, L.group_buf, L.slot_stride, L.active,
                                                    L.n_active, L.offsets, E, L.hq, L.hds, R, d, f,
                                                    L.y, L.ws),

@@ -58,6 +58,18 @@
  *     w = d*q (Q8_0), d*q + m (Q4_1) or d*(c - 2) (Q2_0, code c in 0..3).  The
  *     pages name Q2_0 ([#1368] "Identity") without defining it; this is the
  *     library's own definition.
+ *   Q2_K record matrices (the pages name Q2_K with the D2S6 layout, [#1368]
+ *     "Identity", without defining either; this is the library's definition):
+ *     K % 256 == 0; 256-weight super-blocks of sixteen 16-weight sub-blocks;
+ *     quant plane of 2-bit codes c packed as for Q2_0; then the binary16 d plane
+ *     and the binary16 dmin plane, each [K/256][rows] (super-block-major); then
+ *     one byte per sub-block, [K/16][rows], holding the 4-bit scale sc in the
+ *     low nibble and the 4-bit min mn in the high nibble.  w = d*sc*c - dmin*mn.
+ *   D2S6 q8_1 layout (what MOE_W_Q2_K's MMQ reads): the same q plane, and four
+ *     binary16 per block, ds [rows][width/32][4] = (d, s, s_lo, s_hi) with
+ *     s_lo = fp16(d * sum of q[0..15]) and s_hi = fp16(d * sum of q[16..31])
+ *     (fp32 d, one fp32 product) -- the activation sums of the two 16-weight
+ *     sub-blocks a 32-block spans, which the Q2_K min term multiplies.
  */
 #ifndef MOE_Q8_H
 #define MOE_Q8_H
@@ -79,7 +91,7 @@ typedef enum {
     MOE_ERR_DEVICE = -6       /* moe_device_error found a device-side error bit */
 } moe_status;
 
-typedef enum { MOE_W_Q8_0 = 0, MOE_W_Q4_1 = 1, MOE_W_Q2_0 = 2 } moe_wtype;
+typedef enum { MOE_W_Q8_0 = 0, MOE_W_Q4_1 = 1, MOE_W_Q2_0 = 2, MOE_W_Q2_K = 3 } moe_wtype;
 
 /* Device error bits, set in the workspace error word. */
 #define MOE_DEV_ERR_BAD_EXPERT_ID 0x1u /* an id outside [0, E): its slot is -1 */
@@ -144,6 +156,22 @@ int moe_quantize_gather_q8_1(const float* x, int T, int d, const int32_t* src, i
                              uint16_t* ds, void* stream);
 
 /*
+ * Stage 2 (scatter and gather forms) and stage 5 in the D2S6 layout, the q8_1
+ * rows that MOE_W_Q2_K's MMQ reads ([#1368] "Identity": the scatter writes
+ * the same bytes as the gather in every layout, D2S6 included).  Arguments,
+ * row maps and alignment as moe_quantize_scatter_q8_1,
+ * moe_quantize_gather_q8_1 and moe_requant_hidden_q8_1, except that ds / hds
+ * are uint16 [rows][width/32][4] of (d, s, s_lo, s_hi), 8-byte aligned.  q and
+ * (d, s) are byte-identical to the (d, s) layout's.
+ */
+int moe_quantize_scatter_q8_1_d2s6(const float* x, int T, int d, int K, const int32_t* slot,
+                                   int R, int8_t* q, uint16_t* ds, void* stream);
+int moe_quantize_gather_q8_1_d2s6(const float* x, int T, int d, const int32_t* src, int R,
+                                  int8_t* q, uint16_t* ds, void* stream);
+int moe_requant_hidden_q8_1_d2s6(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
+                                 void* stream);
+
+/*
  * Stage 3 -- [#439] "What" / [#372] "What changes": one launch copies up to 16
  * experts' records into the group buffer, blockIdx.y = expert; expert j of the
  * call lands in slot first_slot + j.  The same bytes as one copy per expert.
@@ -177,11 +205,17 @@ int moe_group_gather_active(const uint8_t* arena, size_t rec_bytes, size_t arena
  *   g[r,j] = sum over blocks b ascending of  dWg[j,b]*dx[r,b]*I_b (+ mWg[j,b]*sx[r,b]
  *            for Q4_1), accumulated in fp32, I_b the exact integer block dot;
  *   u likewise with W_up;  h[r,j] = (g / (1 + exp(-g))) * u.
- *   q int8 [R][d], ds uint16 [R][d/32][2] (stage 2 output); h float [R][f] out.
+ *   Q2_K: block b of super-block u = b/8 spans the sub-blocks 2b and 2b+1;
+ *   I_b = sc_2b * (sum of c*q over its first 16) + sc_2b+1 * (over its last 16),
+ *   the scale is d_u*dx[r,b], and the min term is two more fp32 steps,
+ *   fma(-(dmin_u*mn_2b), s_lo[r,b], acc) then fma(-(dmin_u*mn_2b+1), s_hi[r,b], acc).
+ *   q int8 [R][d], ds uint16 [R][d/32][2] (stage 2 output; [R][d/32][4] in the
+ *   D2S6 layout for MOE_W_Q2_K); h float [R][f] out.
  * group_base and slot_stride must be 128-byte aligned, q, ds and h 16-byte
- * aligned, d % 32 == 0, f % 32 == 0.  Shapes with d % 256 == 0 and f % 128 == 0
- * run on the tensor cores; others on a CUDA-core kernel with the same result.
- * Rows past R are skipped (MOE_DEV_ERR_BAD_ROWS).
+ * aligned, d % 32 == 0, f % 32 == 0 (Q2_K: d % 256 == 0, f % 256 == 0).  Shapes
+ * with d % 256 == 0 and f % 128 == 0 run on the tensor cores; others on a
+ * CUDA-core kernel with the same result.  Rows past R are skipped
+ * (MOE_DEV_ERR_BAD_ROWS).
  */
 int moe_grouped_mmq_gateup(int wtype, const uint8_t* group_base, size_t slot_stride,
                            const int32_t* active, const int32_t* n_active, const int32_t* offsets,
@@ -206,8 +240,8 @@ int moe_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* 
  * ([#439] rebase note, [#1368] "Identity" tests) without defining it; this is
  * our own fusion.  Tensor-core kernel only: returns MOE_ERR_UNSUPPORTED where
  * moe_grouped_mmq_gateup would take the CUDA-core kernel (d % 256 != 0,
- * f % 128 != 0, or MOE_MMQ_PATH=simt).  hds 4-byte aligned; otherwise as
- * stage 4.
+ * f % 128 != 0, or MOE_MMQ_PATH=simt).  hds 4-byte aligned (MOE_W_Q2_K: the
+ * D2S6 layout, 8-byte aligned); otherwise as stage 4.
  */
 int moe_grouped_mmq_gateup_q8_1(int wtype, const uint8_t* group_base, size_t slot_stride,
                                 const int32_t* active, const int32_t* n_active,
@@ -217,8 +251,10 @@ int moe_grouped_mmq_gateup_q8_1(int wtype, const uint8_t* group_base, size_t slo
 
 /*
  * Stage 6 -- grouped quantized matmul, down projection: y[r,i] = sum over
- * blocks b of dWd[i,b]*dh[r,b]*I_b (+ mWd[i,b]*sh[r,b] for Q4_1), fp32.
- *   hq, hds from stage 5; y float [R][d] out.  Alignment as stage 4.
+ * blocks b of dWd[i,b]*dh[r,b]*I_b (+ mWd[i,b]*sh[r,b] for Q4_1; Q2_K as in
+ * stage 4), fp32.
+ *   hq, hds from stage 5 (D2S6 for MOE_W_Q2_K); y float [R][d] out.  Alignment
+ *   and shapes as stage 4.
  */
 int moe_grouped_mmq_down(int wtype, const uint8_t* group_base, size_t slot_stride,
                          const int32_t* active, const int32_t* n_active, const int32_t* offsets,
@@ -312,7 +348,8 @@ int moe_build_slot_map_noalloc(const int32_t* ids, int T, int K, int E, int32_t*
  *     their row offsets, then the per-group expert counts staged for the
  *     device); the caller must not write it while a call is in flight.
  *   - The other buffers as the stage calls document (q, ds for T*K rows of d;
- *     h, hq, hds for T*K rows of f; y for T*K rows of d; ws of
+ *     h, hq, hds for T*K rows of f; ds and hds in the D2S6 layout for
+ *     MOE_W_Q2_K; y for T*K rows of d; ws of
  *     moe_workspace_size(T, K, E, d, f) bytes).
  *   - ring_groups in [1, 64]; compute_stream != copy_stream.
  */

@@ -16,7 +16,12 @@ Recipe (all seeded, counter-based, independent of thread count):
            100 + 3e + m), quantized per 32-wide block of the reduction dimension
            to Q8_0 (d = amax/127, q = round(w/d)), Q4_1 (d = (max-min)/15,
            m = min, q = round((w-m)/d) clamped to [0, 15]) or Q2_0 (d = amax/2,
-           c = round(w/d) + 2 clamped to [0, 3]); scales stored fp16.
+           c = round(w/d) + 2 clamped to [0, 3]); scales stored fp16.  Q2_K packs
+           per 256-wide super-block: each 16-wide sub-block j spans [-mn_j, max_j]
+           (mn_j = max(0, -min)) in three steps st_j = (max_j + mn_j)/3; d =
+           max st_j / 15 and dmin = max mn_j / 15 (fp16); sc_j = round(st_j/d),
+           mn'_j = round(mn_j/dmin) in [0, 15]; c = round((w + dmin*mn'_j) /
+           (d*sc_j)) clamped to [0, 3].
 """
 from __future__ import annotations
 
@@ -35,7 +40,8 @@ LIB = os.path.join(HERE, "libmoe_gen.so")
 Q8_0 = 0
 Q4_1 = 1
 Q2_0 = 2
-WTYPE_NAMES = {Q8_0: "q8_0", Q4_1: "q4_1", Q2_0: "q2_0"}
+Q2_K = 3
+WTYPE_NAMES = {Q8_0: "q8_0", Q4_1: "q4_1", Q2_0: "q2_0", Q2_K: "q2_k"}
 
 _lock = threading.Lock()
 _lib = None
@@ -149,9 +155,11 @@ CONFIGS = {c.name: c for c in [
            zero_every=997),
     Config("T2048_d2048_f768_E512_K10_q2_0", 2048, 2048, 768, 512, 10, Q2_0, 0x5EED0006,
            zero_tokens=(1024,)),
+    Config("T2048_d2048_f768_E512_K10_q2_k", 2048, 2048, 768, 512, 10, Q2_K, 0x5EED0007,
+           zero_tokens=(1500,)),
 ]}
 CONFIG_LIST = list(CONFIGS.values())
-TINY, T600, T2048, T8192, T32768, T2048_Q2 = CONFIG_LIST
+TINY, T600, T2048, T8192, T32768, T2048_Q2, T2048_Q2K = CONFIG_LIST
 
 
 def routing_logits(cfg: Config, tokens: np.ndarray | None = None) -> np.ndarray:

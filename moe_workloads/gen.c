@@ -111,16 +111,27 @@ void gen_normal_f32(uint64_t seed, uint64_t tensor_id, uint64_t start, size_t n,
 /* ---------------- expert records (the library's weight format) --------------- */
 /* gate [f x d], up [f x d], down [d x f]; per matrix: quant plane, fp16 d plane
    [K/32][rows] (block-major), Q4_1 also fp16 m plane [K/32][rows]; planes
-   128-byte aligned.  Quant bytes per row: K (Q8_0), K/2 (Q4_1), K/4 (Q2_0). */
+   128-byte aligned.  Quant bytes per row: K (Q8_0), K/2 (Q4_1), K/4 (Q2_0, Q2_K).
+   Q2_K (wtype 3, K a multiple of 256): 2-bit codes as Q2_0, fp16 d and dmin per
+   256-weight super-block in planes [K/256][rows], and one byte per 16-weight
+   sub-block, scale sc in the low and min mn in the high nibble, plane
+   [K/16][rows]; w = d*sc*c - dmin*mn. */
 static size_t a128(size_t x) { return (x + 127u) & ~(size_t)127u; }
 
-static size_t mat_bytes(int wtype, int rows, int k, size_t* qoff, size_t* doff, size_t* moff) {
-    size_t qb = (size_t)rows * (size_t)k / (wtype == 1 ? 2u : wtype == 2 ? 4u : 1u);
-    size_t sb = (size_t)rows * (size_t)(k / 32) * 2u;
+static size_t mat_bytes4(int wtype, int rows, int k, size_t* qoff, size_t* doff, size_t* moff,
+                         size_t* soff) {
+    size_t qb = (size_t)rows * (size_t)k / (wtype == 1 ? 2u : (wtype == 2 || wtype == 3) ? 4u : 1u);
+    size_t sb = (size_t)rows * (size_t)(k / (wtype == 3 ? 256 : 32)) * 2u;
     *qoff = 0;
     *doff = a128(qb);
     *moff = *doff + a128(sb);
-    return *moff + (wtype == 1 ? a128(sb) : 0u);
+    *soff = *moff + ((wtype == 1 || wtype == 3) ? a128(sb) : 0u);
+    return *soff + (wtype == 3 ? a128((size_t)rows * (size_t)(k / 16)) : 0u);
+}
+
+static size_t mat_bytes(int wtype, int rows, int k, size_t* qoff, size_t* doff, size_t* moff) {
+    size_t soff;
+    return mat_bytes4(wtype, rows, k, qoff, doff, moff, &soff);
 }
 
 size_t gen_record_bytes(int wtype, int d, int f) {
@@ -135,10 +146,65 @@ static uint16_t to_f16_bits(float v) {
     return b;
 }
 
+static float from_f16_bits(uint16_t b) {
+    _Float16 h;
+    memcpy(&h, &b, 2);
+    return (float)h;
+}
+
+/* Q2_K: one 256-weight super-block v of a row.  Per 16-weight sub-block j the
+   codes cover [-mn_j, max_j] in 3 steps; the super-block stores d = max step / 15
+   and dmin = max mn_j / 15 (fp16), each sub-block sc_j = round(step_j / d) and
+   mn_j = round(mn_j / dmin) in [0, 15], and c = round((w + dmin*mn) / (d*sc)) in
+   [0, 3] from the stored (rounded) values. */
+static void pack_q2k_super(const float* v, uint8_t* codes, uint8_t* scmn, int rows, int r,
+                           int sb, uint16_t* dp, uint16_t* mp) {
+    float step[16], mins[16];
+    float smax = 0.0f, mmax = 0.0f;
+    for (int j = 0; j < 16; ++j) {
+        float lo = v[16 * j], hi = v[16 * j];
+        for (int i = 1; i < 16; ++i) {
+            lo = fminf(lo, v[16 * j + i]);
+            hi = fmaxf(hi, v[16 * j + i]);
+        }
+        mins[j] = fmaxf(0.0f, -lo);
+        step[j] = (hi + mins[j]) / 3.0f;
+        smax = fmaxf(smax, step[j]);
+        mmax = fmaxf(mmax, mins[j]);
+    }
+    const uint16_t dbits = to_f16_bits(smax / 15.0f), mbits = to_f16_bits(mmax / 15.0f);
+    const float dd = from_f16_bits(dbits), dm = from_f16_bits(mbits);
+    dp[(size_t)sb * rows + r] = dbits;
+    mp[(size_t)sb * rows + r] = mbits;
+    for (int j = 0; j < 16; ++j) {
+        int sc = dd > 0.0f ? (int)fminf(15.0f, fmaxf(0.0f, roundf(step[j] / dd))) : 0;
+        int mn = dm > 0.0f ? (int)fminf(15.0f, fmaxf(0.0f, roundf(mins[j] / dm))) : 0;
+        scmn[((size_t)sb * 16 + j) * rows + r] = (uint8_t)(sc | (mn << 4));
+        const float s = dd * (float)sc, m = dm * (float)mn;
+        for (int q4 = 0; q4 < 4; ++q4) {  /* four bytes of four codes each */
+            uint8_t byte = 0;
+            for (int i = 0; i < 4; ++i) {
+                const float x = v[16 * j + 4 * q4 + i];
+                int c = s > 0.0f ? (int)fminf(3.0f, fmaxf(0.0f, roundf((x + m) / s))) : 0;
+                byte |= (uint8_t)(c << (2 * i));
+            }
+            codes[16 * j / 4 + q4] = byte;
+        }
+    }
+}
+
 /* Quantize one matrix of weights w [rows x k] into the record at dst. */
 static void pack_matrix(int wtype, const float* w, int rows, int k, uint8_t* dst) {
-    size_t qo, dof, mo;
-    mat_bytes(wtype, rows, k, &qo, &dof, &mo);
+    size_t qo, dof, mo, so;
+    mat_bytes4(wtype, rows, k, &qo, &dof, &mo, &so);
+    if (wtype == 3) {
+        for (int r = 0; r < rows; ++r)
+            for (int sb = 0; sb < k / 256; ++sb)
+                pack_q2k_super(w + (size_t)r * k + (size_t)sb * 256,
+                               dst + qo + (size_t)r * (k / 4) + (size_t)sb * 64, dst + so, rows, r, sb,
+                               (uint16_t*)(dst + dof), (uint16_t*)(dst + mo));
+        return;
+    }
     uint8_t* qp = dst + qo;
     uint16_t* dp = (uint16_t*)(dst + dof);
     uint16_t* mp = (uint16_t*)(dst + mo);
@@ -223,7 +289,7 @@ static void* rec_worker(void* p) {
 }
 
 /* Fill E expert records (arena_stride bytes apart) with N(0, sigma) weights,
-   quantized to wtype (0 = Q8_0, 1 = Q4_1).  Expert e, matrix m (gate, up,
+   quantized to wtype (0 = Q8_0, 1 = Q4_1, 2 = Q2_0, 3 = Q2_K).  Expert e, matrix m (gate, up,
    down) draws from tensor id 100 + 3e + m, element index row*k + col. */
 void gen_expert_records(int wtype, int E, int d, int f, uint64_t seed, double sigma,
                         uint8_t* arena, size_t arena_stride, int threads) {

@@ -6,7 +6,8 @@ tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may load
 it.  It shares no code with the CUDA library and never imports it.
 
 Every wrapper takes and returns numpy arrays; fp16 quantities are carried as
-``uint16`` bit patterns (``ds`` arrays hold ``(d, s)`` pairs along the last axis).
+``uint16`` bit patterns (``ds`` arrays hold ``(d, s)`` pairs along the last axis,
+or ``(d, s, s_lo, s_hi)`` in the D2S6 layout that Q2_K weights read).
 The pages and passages each function follows are cited in ``oracle.c``.
 """
 from __future__ import annotations
@@ -25,7 +26,19 @@ LIB = os.path.join(HERE, "liboracle.so")
 W_Q8_0 = 0
 W_Q4_1 = 1
 W_Q2_0 = 2
+W_Q2_K = 3
 QK = 32
+LAYOUT_DS = 0
+LAYOUT_D2S6 = 1
+
+
+def layout_of(wtype: int) -> int:
+    """The activation layout the MMQ of a weight type reads."""
+    return LAYOUT_D2S6 if wtype == W_Q2_K else LAYOUT_DS
+
+
+def ds_per_block(layout: int) -> int:
+    return 4 if layout == LAYOUT_D2S6 else 2
 
 _lock = threading.Lock()
 _lib = None
@@ -60,9 +73,10 @@ def _load():
                 "oracle_record_offsets": (None, [I, I, I, P, P, P]),
                 "oracle_build_slot_map": (I, [P, I, I, I, P, P, P, P, P]),
                 "oracle_quantize_block_q8_1": (None, [P, P, P, P]),
-                "oracle_quantize_scatter_q8_1": (None, [P, I, I, I, P, P, P]),
-                "oracle_quantize_gather_q8_1": (None, [P, I, P, I, P, P]),
-                "oracle_requant_hidden_q8_1": (None, [P, I, I, P, P]),
+                "oracle_quantize_block_q8_1_d2s6": (None, [P, P, P]),
+                "oracle_quantize_scatter_q8_1": (None, [P, I, I, I, P, P, P, I]),
+                "oracle_quantize_gather_q8_1": (None, [P, I, P, I, P, P, I]),
+                "oracle_requant_hidden_q8_1": (None, [P, I, I, P, P, I]),
                 "oracle_gather_one": (None, [P, Z, Z, I, P, Z, I]),
                 "oracle_group_gather": (None, [P, Z, Z, P, I, I, P, Z]),
                 "oracle_grouped_mmq_gateup": (None, [I, P, Z, P, I, P, P, P, I, I, P]),
@@ -143,37 +157,47 @@ def quantize_block_q8_1(v):
     return q, int(dh[0]), int(sh[0])
 
 
-def quantize_scatter_q8_1(x, slot, K: int, R: int, fill: int = 0):
+def quantize_block_q8_1_d2s6(v):
+    """One block in the D2S6 layout: q int8 [32] and (d, s, s_lo, s_hi) fp16 bits."""
+    v = _c(v, np.float32)
+    assert v.shape == (QK,)
+    q = np.empty(QK, np.int8)
+    e = np.zeros(4, np.uint16)
+    _load().oracle_quantize_block_q8_1_d2s6(_p(v), _p(q), _p(e))
+    return q, e
+
+
+def quantize_scatter_q8_1(x, slot, K: int, R: int, fill: int = 0, layout: int = LAYOUT_DS):
     """Stage a2.  x: f32 [T, d]; slot: int32 [T*K].  Returns q int8 [R, d] and
-    ds uint16 [R, d/32, 2].  Rows nobody writes keep ``fill``."""
+    ds uint16 [R, d/32, ds_per_block(layout)].  Rows nobody writes keep ``fill``."""
     x = _c(x, np.float32)
     slot = _c(slot, np.int32)
     T, d = x.shape
     q = np.full((R, d), fill, np.int8)
-    ds = np.full((R, d // QK, 2), fill, np.uint16)
-    _load().oracle_quantize_scatter_q8_1(_p(x), T, d, K, _p(slot), _p(q), _p(ds))
+    ds = np.full((R, d // QK, ds_per_block(layout)), fill, np.uint16)
+    _load().oracle_quantize_scatter_q8_1(_p(x), T, d, K, _p(slot), _p(q), _p(ds), layout)
     return q, ds
 
 
-def quantize_gather_q8_1(x, src):
+def quantize_gather_q8_1(x, src, layout: int = LAYOUT_DS):
     """Per-row gather quantizer: row r quantizes token src[r]."""
     x = _c(x, np.float32)
     src = _c(src, np.int32)
     d = x.shape[1]
     R = src.shape[0]
     q = np.empty((R, d), np.int8)
-    ds = np.empty((R, d // QK, 2), np.uint16)
-    _load().oracle_quantize_gather_q8_1(_p(x), d, _p(src), R, _p(q), _p(ds))
+    ds = np.empty((R, d // QK, ds_per_block(layout)), np.uint16)
+    _load().oracle_quantize_gather_q8_1(_p(x), d, _p(src), R, _p(q), _p(ds), layout)
     return q, ds
 
 
-def requant_hidden_q8_1(h):
-    """Stage a5.  h: f32 [R, f] -> hq int8 [R, f], hds uint16 [R, f/32, 2]."""
+def requant_hidden_q8_1(h, layout: int = LAYOUT_DS):
+    """Stage a5.  h: f32 [R, f] -> hq int8 [R, f], hds uint16 [R, f/32, ds_per_block(layout)]."""
     h = _c(h, np.float32)
     R, f = h.shape
     hq = np.empty((R, f), np.int8)
-    hds = np.empty((R, f // QK, 2), np.uint16)
-    _load().oracle_requant_hidden_q8_1(_p(h), R, f, _p(hq), _p(hds))
+    hds = np.empty((R, f // QK, ds_per_block(layout)), np.uint16)
+    _load().oracle_requant_hidden_q8_1(_p(h), R, f, _p(hq), _p(hds), layout)
     return hq, hds
 
 
@@ -245,12 +269,13 @@ def layer_forward(wtype, arena, rec_bytes, arena_stride, x, ids, w, E, d, f, slo
     K = ids.shape[1]
     sm = build_slot_map(ids, E)
     R = int(sm["offsets"][E])
-    q, ds = quantize_scatter_q8_1(x, sm["slot"], K, R)
+    lay = layout_of(wtype)
+    q, ds = quantize_scatter_q8_1(x, sm["slot"], K, R, layout=lay)
     slot_stride = slot_stride or rec_bytes
     gb = gather_groups(arena, rec_bytes, arena_stride, sm["active"], sm["n_active"], slot_stride)
     h = grouped_mmq_gateup(wtype, gb, slot_stride, sm["active"], sm["n_active"], sm["offsets"],
                            q, ds, d, f)
-    hq, hds = requant_hidden_q8_1(h)
+    hq, hds = requant_hidden_q8_1(h, layout=lay)
     y = grouped_mmq_down(wtype, gb, slot_stride, sm["active"], sm["n_active"], sm["offsets"],
                          hq, hds, d, f)
     out = combine_topk(y, sm["slot"], w, T, K, d)

@@ -39,6 +39,20 @@
  *                     (four per byte: element 4j+i of a block in bits 2i..2i+1 of
  *                     byte j), fp16 d, w = d*(c - 2), so the block dot uses the
  *                     integers c - 2 in {-2, -1, 0, 1} and no m term.
+ *   Q2_K weights:     named by "#1368 ..." (section "Identity": the D2S6
+ *                     activation layout serves Q2_K) but not defined there; this
+ *                     library's definition: 256-weight super-blocks, each of
+ *                     sixteen 16-weight sub-blocks; 2-bit codes c packed as for
+ *                     Q2_0; per super-block fp16 d and fp16 dmin; per sub-block
+ *                     one byte holding a 4-bit scale sc (low nibble) and a 4-bit
+ *                     min mn (high nibble); w = d*sc*c - dmin*mn.
+ *   D2S6 layout:      the pages name it for Q2_K without defining it.  This
+ *                     library's reading: the same q8_1 quants and d as above,
+ *                     with four fp16 per 32-block, (d, s, s_lo, s_hi), where
+ *                     s_lo = d * sum(q[0..15]) and s_hi = d * sum(q[16..31]) (fp32
+ *                     d, one fp32 product, rounded to fp16): the Q2_K min term
+ *                     needs the activation sum of every 16-weight sub-block.
+ *                     The other weight types use (d, s) pairs.
  *   Gate/up product:  h = SiLU(g) * u with SiLU(g) = g / (1 + exp(-g)).
  *
  * Parity pins for every function are in tests/test_oracle_pins.py.
@@ -49,13 +63,24 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define QK 32 /* block width of q8_1, Q8_0, Q4_1 and Q2_0 */
+#define QK 32   /* block width of q8_1, Q8_0, Q4_1 and Q2_0 */
+#define QKK 256 /* Q2_K super-block width */
 
-enum { ORACLE_W_Q8_0 = 0, ORACLE_W_Q4_1 = 1, ORACLE_W_Q2_0 = 2 };
+enum { ORACLE_W_Q8_0 = 0, ORACLE_W_Q4_1 = 1, ORACLE_W_Q2_0 = 2, ORACLE_W_Q2_K = 3 };
+enum { ORACLE_LAYOUT_DS = 0, ORACLE_LAYOUT_D2S6 = 1 };
 
 /* quant bytes per row of a matrix with reduction length k */
 static size_t quant_row_bytes(int wtype, int k) {
-    return (size_t)k / (wtype == ORACLE_W_Q4_1 ? 2u : wtype == ORACLE_W_Q2_0 ? 4u : 1u);
+    return (size_t)k / (wtype == ORACLE_W_Q4_1 ? 2u
+                        : (wtype == ORACLE_W_Q2_0 || wtype == ORACLE_W_Q2_K) ? 4u : 1u);
+}
+
+/* fp16 entries per 32-block in an activation ds row: (d, s) or (d, s, s_lo, s_hi) */
+static int ds_per_block(int layout) { return layout == ORACLE_LAYOUT_D2S6 ? 4 : 2; }
+
+/* the activation layout the MMQ of a weight type reads */
+static int layout_of(int wtype) {
+    return wtype == ORACLE_W_Q2_K ? ORACLE_LAYOUT_D2S6 : ORACLE_LAYOUT_DS;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -129,22 +154,25 @@ void oracle_f16_to_f32_array(const uint16_t* in, size_t n, float* out) {
 /* down [d x f]; each matrix is the plane of quants (row-major, reduction dim */
 /* innermost), then the fp16 d plane [K/32][rows] (block-major), then for     */
 /* Q4_1 the fp16 m plane [K/32][rows]; every plane starts on a 128-byte       */
-/* boundary.                                                                  */
+/* boundary.  Q2_K: quants, then fp16 d [K/256][rows], fp16 dmin             */
+/* [K/256][rows] and the sub-block byte plane (sc | mn << 4) [K/16][rows].    */
 /* ------------------------------------------------------------------------- */
 static size_t align128(size_t x) { return (x + 127u) & ~(size_t)127u; }
 
 typedef struct {
-    size_t q, d, m, bytes; /* plane offsets inside the matrix, matrix size */
+    size_t q, d, m, s, bytes; /* plane offsets inside the matrix, matrix size */
 } oracle_matrix_layout;
 
 static oracle_matrix_layout matrix_layout(int wtype, int rows, int k) {
     oracle_matrix_layout L;
     size_t qbytes = (size_t)rows * quant_row_bytes(wtype, k);
-    size_t sbytes = (size_t)rows * (size_t)(k / QK) * 2u;
+    size_t sbytes = (size_t)rows * (size_t)(k / (wtype == ORACLE_W_Q2_K ? QKK : QK)) * 2u;
+    int has_m = wtype == ORACLE_W_Q4_1 || wtype == ORACLE_W_Q2_K;
     L.q = 0;
     L.d = align128(qbytes);
     L.m = L.d + align128(sbytes);
-    L.bytes = L.m + (wtype == ORACLE_W_Q4_1 ? align128(sbytes) : 0u);
+    L.s = L.m + (has_m ? align128(sbytes) : 0u);
+    L.bytes = L.s + (wtype == ORACLE_W_Q2_K ? align128((size_t)rows * (size_t)(k / 16)) : 0u);
     return L;
 }
 
@@ -214,8 +242,11 @@ int oracle_build_slot_map(const int32_t* ids, int T, int K, int E, int32_t* offs
 /*   or amax <= 63 * 2^-149 so that the quotient underflows) then q = 0,       */
 /*   d = 0, s = 0; else q_i = round-half-away(v_i / d) (IEEE),                 */
 /*   S = sum q_i exactly, stored d_h = fp16(d), s_h = fp16(d * S).            */
+/*   Every quantizer below takes the activation layout: ORACLE_LAYOUT_DS      */
+/*   ((d, s) per block) or ORACLE_LAYOUT_D2S6 ((d, s, s_lo, s_hi)).           */
 /* ------------------------------------------------------------------------- */
-void oracle_quantize_block_q8_1(const float* v, int8_t* q, uint16_t* dh, uint16_t* sh) {
+/* The quants of one block; returns the fp32 d (0 for an all-zero block). */
+static float block_quants(const float* v, int8_t* q) {
     float amax = 0.0f;
     for (int i = 0; i < QK; ++i) {
         float a = fabsf(v[i]);
@@ -224,39 +255,61 @@ void oracle_quantize_block_q8_1(const float* v, int8_t* q, uint16_t* dh, uint16_
     float d = amax / 127.0f;
     if (d == 0.0f) {  /* x / d is undefined: the block is stored as all-zero */
         for (int i = 0; i < QK; ++i) q[i] = 0;
-        *dh = 0;
-        *sh = 0;
-        return;
+        return 0.0f;
     }
-    int sum = 0;
     for (int i = 0; i < QK; ++i) {
         float r = roundf(v[i] / d);
         if (r > 127.0f) r = 127.0f;
         if (r < -127.0f) r = -127.0f;
         q[i] = (int8_t)r;
-        sum += q[i];
     }
-    *dh = oracle_f32_to_f16(d);
-    *sh = oracle_f32_to_f16(d * (float)sum);
+    return d;
 }
 
-/* Quantize one row of n values (n % 32 == 0) into q[n] and ds[2*(n/32)]
-   (ds holds (d, s) pairs of fp16 bit patterns). */
-static void quantize_row(const float* x, int n, int8_t* q, uint16_t* ds) {
-    for (int b = 0; b < n / QK; ++b)
-        oracle_quantize_block_q8_1(x + b * QK, q + b * QK, &ds[2 * b], &ds[2 * b + 1]);
+static int sum_quants(const int8_t* q, int from, int to) {
+    int sum = 0;
+    for (int i = from; i < to; ++i) sum += q[i];
+    return sum;
+}
+
+void oracle_quantize_block_q8_1(const float* v, int8_t* q, uint16_t* dh, uint16_t* sh) {
+    float d = block_quants(v, q);
+    *dh = oracle_f32_to_f16(d);
+    *sh = oracle_f32_to_f16(d * (float)sum_quants(q, 0, QK));
+}
+
+/* The D2S6 reading of the block: e[0..3] = fp16 of d, d*S, d*S_lo, d*S_hi with
+   S_lo, S_hi the exact sums of q over elements 0..15 and 16..31. */
+void oracle_quantize_block_q8_1_d2s6(const float* v, int8_t* q, uint16_t* e) {
+    float d = block_quants(v, q);
+    e[0] = oracle_f32_to_f16(d);
+    e[1] = oracle_f32_to_f16(d * (float)sum_quants(q, 0, QK));
+    e[2] = oracle_f32_to_f16(d * (float)sum_quants(q, 0, QK / 2));
+    e[3] = oracle_f32_to_f16(d * (float)sum_quants(q, QK / 2, QK));
+}
+
+/* Quantize one row of n values (n % 32 == 0) into q[n] and ds, the row's fp16
+   bit patterns, ds_per_block(layout) per block. */
+static void quantize_row(const float* x, int n, int8_t* q, uint16_t* ds, int layout) {
+    int w = ds_per_block(layout);
+    for (int b = 0; b < n / QK; ++b) {
+        if (layout == ORACLE_LAYOUT_D2S6)
+            oracle_quantize_block_q8_1_d2s6(x + b * QK, q + b * QK, &ds[w * b]);
+        else
+            oracle_quantize_block_q8_1(x + b * QK, q + b * QK, &ds[w * b], &ds[w * b + 1]);
+    }
 }
 
 /* [#1368] intro: quantize each token once, write its blocks to all K of its
    rows through the inverse map.  Rows with slot -1 are skipped. */
 void oracle_quantize_scatter_q8_1(const float* x, int T, int d, int K, const int32_t* slot,
-                                  int8_t* q, uint16_t* ds) {
-    int nb = d / QK;
+                                  int8_t* q, uint16_t* ds, int layout) {
+    size_t row_ds = (size_t)ds_per_block(layout) * (size_t)(d / QK);
     for (int t = 0; t < T; ++t) {
         for (int k = 0; k < K; ++k) {
             int r = slot[t * K + k];
             if (r < 0) continue;
-            quantize_row(x + (size_t)t * d, d, q + (size_t)r * d, ds + (size_t)r * 2 * nb);
+            quantize_row(x + (size_t)t * d, d, q + (size_t)r * d, ds + (size_t)r * row_ds, layout);
         }
     }
 }
@@ -264,18 +317,19 @@ void oracle_quantize_scatter_q8_1(const float* x, int T, int d, int K, const int
 /* [#1368] intro: the per-row gather quantizer, mmq::quantize(x, src, ...):
    row r reads and quantizes token src[r]; the same bytes as the scatter. */
 void oracle_quantize_gather_q8_1(const float* x, int d, const int32_t* src, int R, int8_t* q,
-                                 uint16_t* ds) {
-    int nb = d / QK;
+                                 uint16_t* ds, int layout) {
+    size_t row_ds = (size_t)ds_per_block(layout) * (size_t)(d / QK);
     for (int r = 0; r < R; ++r)
-        quantize_row(x + (size_t)src[r] * d, d, q + (size_t)r * d, ds + (size_t)r * 2 * nb);
+        quantize_row(x + (size_t)src[r] * d, d, q + (size_t)r * d, ds + (size_t)r * row_ds, layout);
 }
 
 /* Stage a5: the down-projection q8_1 quantization of the hidden rows
    ([#1368] intro names it as unchanged), identity row map. */
-void oracle_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* hds) {
-    int nb = f / QK;
+void oracle_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
+                                int layout) {
+    size_t row_ds = (size_t)ds_per_block(layout) * (size_t)(f / QK);
     for (int r = 0; r < R; ++r)
-        quantize_row(h + (size_t)r * f, f, hq + (size_t)r * f, hds + (size_t)r * 2 * nb);
+        quantize_row(h + (size_t)r * f, f, hq + (size_t)r * f, hds + (size_t)r * row_ds, layout);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -302,43 +356,17 @@ void oracle_group_gather(const uint8_t* arena, size_t rec_bytes, size_t arena_st
 /*         fmaf(fp32(dW[b]) * fp32(dX[b]), (float)I_b, acc)                    */
 /*         and, for Q4_1, then fmaf(fp32(mW[b]), fp32(sX[b]), acc),            */
 /*   with I_b the exact integer sum over the block of qW * qX.                 */
+/*   Q2_K (block b lies in super-block u = b/8 and covers the sub-blocks      */
+/*   2b and 2b+1): I_b = sc_2b * sum_{i<16} c_i qX_i + sc_2b+1 * sum_{i>=16}   */
+/*   c_i qX_i, dW = d_u, and the min term is two more steps,                   */
+/*   fmaf(-(dmin_u * mn_2b), s_lo[b], acc) then fmaf(-(dmin_u * mn_2b+1),      */
+/*   s_hi[b], acc) (each product dmin * mn is exact in fp32).                  */
 /* ------------------------------------------------------------------------- */
-static float mmq_dot(int wtype, const uint8_t* wq_row, const uint16_t* wd, const uint16_t* wm,
-                     size_t sstride, const int8_t* xq_row, const uint16_t* xds_row, int k) {
-    /* wd / wm point at block 0 of this row; block b is sstride entries further */
-    float acc = 0.0f;
-    for (int b = 0; b < k / QK; ++b) {
-        int32_t I = 0;
-        const int8_t* xb = xq_row + b * QK;
-        if (wtype == ORACLE_W_Q8_0) {
-            const int8_t* wb = (const int8_t*)wq_row + b * QK;
-            for (int i = 0; i < QK; ++i) I += (int32_t)wb[i] * (int32_t)xb[i];
-        } else if (wtype == ORACLE_W_Q2_0) {
-            const uint8_t* wb = wq_row + b * (QK / 4);
-            for (int i = 0; i < QK; ++i) {
-                int32_t c = (wb[i / 4] >> (2 * (i % 4))) & 3;
-                I += (c - 2) * (int32_t)xb[i];
-            }
-        } else {
-            const uint8_t* wb = wq_row + b * (QK / 2);
-            for (int j = 0; j < QK / 2; ++j) {
-                int32_t lo = wb[j] & 0x0F, hi = wb[j] >> 4;
-                I += lo * (int32_t)xb[2 * j] + hi * (int32_t)xb[2 * j + 1];
-            }
-        }
-        float scale = oracle_f16_to_f32(wd[(size_t)b * sstride]) * oracle_f16_to_f32(xds_row[2 * b]);
-        acc = fmaf(scale, (float)I, acc);
-        if (wtype == ORACLE_W_Q4_1)
-            acc = fmaf(oracle_f16_to_f32(wm[(size_t)b * sstride]), oracle_f16_to_f32(xds_row[2 * b + 1]),
-                       acc);
-    }
-    return acc;
-}
-
 typedef struct {
     const uint8_t* q;
     const uint16_t* d;
     const uint16_t* m;
+    const uint8_t* s;
     size_t q_row; /* bytes per row of the quant plane */
     int rows;     /* rows of the matrix = stride between blocks of a scale plane */
 } wmat;
@@ -349,13 +377,64 @@ static wmat weight_matrix(int wtype, const uint8_t* base, int rows, int k) {
     W.q = base + L.q;
     W.d = (const uint16_t*)(base + L.d);
     W.m = (const uint16_t*)(base + L.m);
+    W.s = base + L.s;
     W.q_row = quant_row_bytes(wtype, k);
     W.rows = rows;
     return W;
 }
 
+/* 2-bit code of element i of a packed row segment (four per byte, low bits first) */
+static int32_t code2(const uint8_t* p, int i) { return (p[i / 4] >> (2 * (i % 4))) & 3; }
+
+/* Weight row j of W against one activation row (quants xq, fp16 entries xds,
+   ds_per_block(layout_of(wtype)) per block), reduction length k. */
 static float wdot(int wtype, wmat W, int j, const int8_t* xq, const uint16_t* xds, int k) {
-    return mmq_dot(wtype, W.q + (size_t)j * W.q_row, W.d + j, W.m + j, (size_t)W.rows, xq, xds, k);
+    const uint8_t* wq_row = W.q + (size_t)j * W.q_row;
+    const size_t rs = (size_t)W.rows; /* block-major scale planes: entry b of row j at b*rows+j */
+    const int w = ds_per_block(layout_of(wtype));
+    float acc = 0.0f;
+    for (int b = 0; b < k / QK; ++b) {
+        int32_t I = 0;
+        const int8_t* xb = xq + b * QK;
+        if (wtype == ORACLE_W_Q8_0) {
+            const int8_t* wb = (const int8_t*)wq_row + b * QK;
+            for (int i = 0; i < QK; ++i) I += (int32_t)wb[i] * (int32_t)xb[i];
+        } else if (wtype == ORACLE_W_Q2_0) {
+            const uint8_t* wb = wq_row + b * (QK / 4);
+            for (int i = 0; i < QK; ++i) I += (code2(wb, i) - 2) * (int32_t)xb[i];
+        } else if (wtype == ORACLE_W_Q2_K) {
+            const uint8_t* wb = wq_row + b * (QK / 4);
+            for (int h = 0; h < 2; ++h) {
+                int32_t sc = W.s[(size_t)(2 * b + h) * rs + j] & 0x0F;
+                int32_t part = 0;
+                for (int i = 16 * h; i < 16 * h + 16; ++i) part += code2(wb, i) * (int32_t)xb[i];
+                I += sc * part;
+            }
+        } else {
+            const uint8_t* wb = wq_row + b * (QK / 2);
+            for (int i = 0; i < QK / 2; ++i) {
+                int32_t lo = wb[i] & 0x0F, hi = wb[i] >> 4;
+                I += lo * (int32_t)xb[2 * i] + hi * (int32_t)xb[2 * i + 1];
+            }
+        }
+        const uint16_t* e = xds + (size_t)w * b; /* this block's activation entries */
+        if (wtype == ORACLE_W_Q2_K) {
+            const int u = b / (QKK / QK);
+            float scale = oracle_f16_to_f32(W.d[(size_t)u * rs + j]) * oracle_f16_to_f32(e[0]);
+            acc = fmaf(scale, (float)I, acc);
+            const float dmin = oracle_f16_to_f32(W.m[(size_t)u * rs + j]);
+            for (int h = 0; h < 2; ++h) {
+                int32_t mn = W.s[(size_t)(2 * b + h) * rs + j] >> 4;
+                acc = fmaf(-(dmin * (float)mn), oracle_f16_to_f32(e[2 + h]), acc);
+            }
+            continue;
+        }
+        float scale = oracle_f16_to_f32(W.d[(size_t)b * rs + j]) * oracle_f16_to_f32(e[0]);
+        acc = fmaf(scale, (float)I, acc);
+        if (wtype == ORACLE_W_Q4_1)
+            acc = fmaf(oracle_f16_to_f32(W.m[(size_t)b * rs + j]), oracle_f16_to_f32(e[1]), acc);
+    }
+    return acc;
 }
 
 /* SiLU(g) * u in fp32, SiLU(g) = g / (1 + exp(-g)). */
@@ -369,7 +448,7 @@ void oracle_grouped_mmq_gateup(int wtype, const uint8_t* group_base, size_t slot
                                const int8_t* q, const uint16_t* ds, int d, int f, float* h) {
     size_t og, ou, od;
     oracle_record_offsets(wtype, d, f, &og, &ou, &od);
-    int nbx = d / QK;
+    size_t row_ds = (size_t)ds_per_block(layout_of(wtype)) * (size_t)(d / QK);
     for (int p = 0; p < n_active; ++p) {
         int e = active[p];
         const uint8_t* rec = group_base + (size_t)p * slot_stride;
@@ -377,7 +456,7 @@ void oracle_grouped_mmq_gateup(int wtype, const uint8_t* group_base, size_t slot
         wmat U = weight_matrix(wtype, rec + ou, f, d);
         for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
             const int8_t* xq = q + (size_t)r * d;
-            const uint16_t* xds = ds + (size_t)r * 2 * nbx;
+            const uint16_t* xds = ds + (size_t)r * row_ds;
             for (int j = 0; j < f; ++j) {
                 float g = wdot(wtype, G, j, xq, xds, d);
                 float u = wdot(wtype, U, j, xq, xds, d);
@@ -393,14 +472,14 @@ void oracle_grouped_mmq_down(int wtype, const uint8_t* group_base, size_t slot_s
                              const int8_t* hq, const uint16_t* hds, int d, int f, float* y) {
     size_t og, ou, od;
     oracle_record_offsets(wtype, d, f, &og, &ou, &od);
-    int nbh = f / QK;
+    size_t row_ds = (size_t)ds_per_block(layout_of(wtype)) * (size_t)(f / QK);
     for (int p = 0; p < n_active; ++p) {
         int e = active[p];
         const uint8_t* rec = group_base + (size_t)p * slot_stride;
         wmat D = weight_matrix(wtype, rec + od, d, f);
         for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
             const int8_t* xq = hq + (size_t)r * f;
-            const uint16_t* xds = hds + (size_t)r * 2 * nbh;
+            const uint16_t* xds = hds + (size_t)r * row_ds;
             for (int i = 0; i < d; ++i) y[(size_t)r * d + i] = wdot(wtype, D, i, xq, xds, f);
         }
     }

@@ -24,7 +24,14 @@ LIB_PATH = os.path.join(HERE, "libmoe_q8.so")
 MOE_W_Q8_0 = 0
 MOE_W_Q4_1 = 1
 MOE_W_Q2_0 = 2
+MOE_W_Q2_K = 3
 QK = 32
+
+
+def ds_halves(wtype: int) -> int:
+    """binary16 entries per 32-block of a q8_1 ds row for a weight type's MMQ:
+    (d, s), or (d, s, s_lo, s_hi) -- the D2S6 layout -- for Q2_K."""
+    return 4 if wtype == MOE_W_Q2_K else 2
 
 DEV_ERR_BAD_EXPERT_ID = 0x1
 DEV_ERR_BAD_ROWS = 0x2
@@ -45,6 +52,9 @@ _SIGNATURES = {
     "moe_build_slot_map": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_quantize_scatter_q8_1": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "moe_quantize_gather_q8_1": (_I, [_P, _I, _I, _P, _I, _P, _P, _P]),
+    "moe_quantize_scatter_q8_1_d2s6": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "moe_quantize_gather_q8_1_d2s6": (_I, [_P, _I, _I, _P, _I, _P, _P, _P]),
+    "moe_requant_hidden_q8_1_d2s6": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_group_gather": (_I, [_P, _Z, _Z, _P, _I, _I, _P, _Z, _P]),
     "moe_group_gather_active": (_I, [_P, _Z, _Z, _P, _P, _I, _P, _Z, _P]),
     "moe_grouped_mmq_gateup": (_I, [_I, _P, _Z, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _P, _Z, _P]),
@@ -155,6 +165,35 @@ def moe_quantize_gather_q8_1(x, src, R, q, ds, stream=None):
     T, d = x.shape
     _check(lib().moe_quantize_gather_q8_1(_p(x), T, d, _p(src), R, _p(q), _p(ds), _s(stream)),
            "moe_quantize_gather_q8_1")
+
+
+def moe_quantize_scatter_q8_1_d2s6(x, slot, K, R, q, ds, stream=None):
+    _dev(x, slot, q, ds)
+    T, d = x.shape
+    _check(lib().moe_quantize_scatter_q8_1_d2s6(_p(x), T, d, K, _p(slot), R, _p(q), _p(ds),
+                                                _s(stream)), "moe_quantize_scatter_q8_1_d2s6")
+
+
+def moe_quantize_gather_q8_1_d2s6(x, src, R, q, ds, stream=None):
+    _dev(x, src, q, ds)
+    T, d = x.shape
+    _check(lib().moe_quantize_gather_q8_1_d2s6(_p(x), T, d, _p(src), R, _p(q), _p(ds),
+                                               _s(stream)), "moe_quantize_gather_q8_1_d2s6")
+
+
+def quantizers(wtype: int):
+    """(scatter, gather, requant) entry points whose ds layout the weight type's
+    MMQ reads: the D2S6 ones for Q2_K, the (d, s) ones otherwise."""
+    if wtype == MOE_W_Q2_K:
+        return (moe_quantize_scatter_q8_1_d2s6, moe_quantize_gather_q8_1_d2s6,
+                moe_requant_hidden_q8_1_d2s6)
+    return moe_quantize_scatter_q8_1, moe_quantize_gather_q8_1, moe_requant_hidden_q8_1
+
+
+def moe_requant_hidden_q8_1_d2s6(h, R, f, hq, hds, stream=None):
+    _dev(h, hq, hds)
+    _check(lib().moe_requant_hidden_q8_1_d2s6(_p(h), R, f, _p(hq), _p(hds), _s(stream)),
+           "moe_requant_hidden_q8_1_d2s6")
 
 
 def moe_group_gather(arena, rec_bytes, arena_stride, expert_ids, first_slot, group_buf,
@@ -296,11 +335,12 @@ class MoeLayer:
         self.active = torch.zeros(E, **i32)
         self.n_active = torch.zeros(1, **i32)
         self.q = torch.zeros((max(R, 1), d), dtype=torch.int8, device=device)
-        self.ds = torch.zeros((max(R, 1), d // QK, 2), dtype=torch.int16, device=device)
+        hw = ds_halves(wtype)
+        self.ds = torch.zeros((max(R, 1), d // QK, hw), dtype=torch.int16, device=device)
         self.group_buf = torch.zeros(E * self.slot_stride, dtype=torch.uint8, device=device)
         self.h = torch.zeros((max(R, 1), f), dtype=torch.float32, device=device)
         self.hq = torch.zeros((max(R, 1), f), dtype=torch.int8, device=device)
-        self.hds = torch.zeros((max(R, 1), f // QK, 2), dtype=torch.int16, device=device)
+        self.hds = torch.zeros((max(R, 1), f // QK, hw), dtype=torch.int16, device=device)
         self.y = torch.zeros((max(R, 1), d), dtype=torch.float32, device=device)
         self.out = torch.zeros((max(T_max, 1), d), dtype=torch.float32, device=device)
         ws_bytes = moe_workspace_size(T_max, K, E, d, f)
@@ -317,7 +357,8 @@ class MoeLayer:
         R = T * K
         moe_build_slot_map(ids, E, self.offsets, self.slot, self.src, self.active, self.n_active,
                            self.ws, stream)
-        moe_quantize_scatter_q8_1(x, self.slot, K, R, self.q, self.ds, stream)
+        scatter, _, requant = quantizers(self.wtype)
+        scatter(x, self.slot, K, R, self.q, self.ds, stream)
         moe_group_gather_active(self.arena, self.rec_bytes, self.arena_stride, self.active,
                                 self.n_active, E, self.group_buf, self.slot_stride, stream)
         if fused:
@@ -332,7 +373,7 @@ class MoeLayer:
         moe_grouped_mmq_gateup(self.wtype, self.group_buf, self.slot_stride, self.active,
                                self.n_active, self.offsets, E, self.q, self.ds, R, d, f, self.h,
                                self.ws, stream)
-        moe_requant_hidden_q8_1(self.h, R, f, self.hq, self.hds, stream)
+        requant(self.h, R, f, self.hq, self.hds, stream)
         moe_grouped_mmq_down(self.wtype, self.group_buf, self.slot_stride, self.active,
                              self.n_active, self.offsets, E, self.hq, self.hds, R, d, f, self.y,
                              self.ws, stream)

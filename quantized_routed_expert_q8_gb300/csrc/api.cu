@@ -11,10 +11,10 @@ namespace moe {
 int launch_build_slot_map(const int32_t*, int, int, int, int32_t*, int32_t*, int32_t*, int32_t*,
                           int32_t*, uint8_t*, cudaStream_t);
 int launch_quantize_scatter(const float*, int, int, int, const int32_t*, int, int8_t*, uint16_t*,
-                            cudaStream_t);
-int launch_quantize_gather(const float*, int, int, const int32_t*, int, int8_t*, uint16_t*,
+                            bool, cudaStream_t);
+int launch_quantize_gather(const float*, int, int, const int32_t*, int, int8_t*, uint16_t*, bool,
                            cudaStream_t);
-int launch_requant_hidden(const float*, int, int, int8_t*, uint16_t*, cudaStream_t);
+int launch_requant_hidden(const float*, int, int, int8_t*, uint16_t*, bool, cudaStream_t);
 int launch_group_gather(const uint8_t*, size_t, size_t, const int32_t*, int, int, uint8_t*, size_t,
                         cudaStream_t);
 int launch_group_gather_active(const uint8_t*, size_t, size_t, const int32_t*, const int32_t*, int,
@@ -43,7 +43,14 @@ namespace {
 
 inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline bool al(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
-inline bool wtype_ok(int w) { return w == MOE_W_Q8_0 || w == MOE_W_Q4_1 || w == MOE_W_Q2_0; }
+inline bool wtype_ok(int w) {
+    return w == MOE_W_Q8_0 || w == MOE_W_Q4_1 || w == MOE_W_Q2_0 || w == MOE_W_Q2_K;
+}
+// reduction widths a weight type's blocks need: 32, or Q2_K's 256-weight super-blocks
+inline bool widths_ok(int w, int d, int f) {
+    const int b = w == MOE_W_Q2_K ? QKK : QK;
+    return d % b == 0 && f % b == 0;
+}
 
 // Kernel choice for the grouped MMQ.  Stage 4 (gate/up) runs on the tensor-core
 // kernel that forms each block's integer dot exactly and scales it on the CUDA
@@ -77,14 +84,14 @@ int mmq_common(int wtype, bool gateup, const uint8_t* group_base, size_t slot_st
                size_t ws_bytes, void* stream, const MmqFused* F = nullptr, size_t ws_need = 0) {
     if (!wtype_ok(wtype) || R < 0 || d <= 0 || f <= 0 || E <= 0 || E > MAX_E)
         return MOE_ERR_INVALID_ARG;
-    if (d % QK || f % QK) return MOE_ERR_INVALID_ARG;
+    if (!widths_ok(wtype, d, f)) return MOE_ERR_INVALID_ARG;
     if (!active || !n_active || !offsets) return MOE_ERR_INVALID_ARG;
     const bool q8_out = F && F->hq;
     if (R > 0 && (!group_base || !xq || !xds || (!out && !q8_out))) return MOE_ERR_INVALID_ARG;
     if (q8_out && R > 0 && !F->hds) return MOE_ERR_INVALID_ARG;
     if (!al(group_base, 128) || slot_stride % 128) return MOE_ERR_ALIGNMENT;
     if (!al(xq, 16) || !al(xds, 16) || !al(out, 16)) return MOE_ERR_ALIGNMENT;
-    if (q8_out && !al(F->hds, 4)) return MOE_ERR_ALIGNMENT;
+    if (q8_out && !al(F->hds, ds_halves(wtype) == 4 ? 8 : 4)) return MOE_ERR_ALIGNMENT;
     // the tile list needs R/16 + E entries: size it as if T*K = R
     WsLayout W = ws_layout(R, 1, E, d, f);
     int rc = check_ws(ws, ws_bytes, W.core > ws_need ? W.core : ws_need);
@@ -110,7 +117,7 @@ int mmq_common(int wtype, bool gateup, const uint8_t* group_base, size_t slot_st
 extern "C" {
 
 size_t moe_expert_record_bytes(int wtype, int d, int f) {
-    if (!wtype_ok(wtype) || d <= 0 || f <= 0 || d % QK || f % QK) return 0;
+    if (!wtype_ok(wtype) || d <= 0 || f <= 0 || !widths_ok(wtype, d, f)) return 0;
     return rec_layout(wtype, d, f).bytes;
 }
 
@@ -146,23 +153,60 @@ int moe_build_slot_map(const int32_t* ids, int T, int K, int E, int32_t* offsets
                                  S(stream));
 }
 
-int moe_quantize_scatter_q8_1(const float* x, int T, int d, int K, const int32_t* slot, int R,
-                              int8_t* q, uint16_t* ds, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int quantize_scatter(const float* x, int T, int d, int K, const int32_t* slot, int R, int8_t* q,
+                     uint16_t* ds, bool d2s6, void* stream) {
     if (T < 0 || K < 0 || R < 0 || d <= 0 || d % QK) return MOE_ERR_INVALID_ARG;
     if ((long long)T * K > 0 && (!x || !slot)) return MOE_ERR_INVALID_ARG;
     if (R > 0 && (!q || !ds)) return MOE_ERR_INVALID_ARG;
-    if (!al(x, 16) || !al(q, 16) || !al(ds, 4)) return MOE_ERR_ALIGNMENT;
+    if (!al(x, 16) || !al(q, 16) || !al(ds, d2s6 ? 8 : 4)) return MOE_ERR_ALIGNMENT;
     if (T == 0 || K == 0 || R == 0) return MOE_OK;
-    return launch_quantize_scatter(x, T, d, K, slot, R, q, ds, S(stream));
+    return launch_quantize_scatter(x, T, d, K, slot, R, q, ds, d2s6, S(stream));
+}
+
+int quantize_gather(const float* x, int T, int d, const int32_t* src, int R, int8_t* q,
+                    uint16_t* ds, bool d2s6, void* stream) {
+    if (T < 0 || R < 0 || d <= 0 || d % QK) return MOE_ERR_INVALID_ARG;
+    if (R > 0 && (!x || !src || !q || !ds)) return MOE_ERR_INVALID_ARG;
+    if (!al(x, 16) || !al(q, 16) || !al(ds, d2s6 ? 8 : 4)) return MOE_ERR_ALIGNMENT;
+    if (R == 0) return MOE_OK;
+    return launch_quantize_gather(x, T, d, src, R, q, ds, d2s6, S(stream));
+}
+
+int requant_hidden(const float* h, int R, int f, int8_t* hq, uint16_t* hds, bool d2s6,
+                   void* stream) {
+    if (R < 0 || f <= 0 || f % QK) return MOE_ERR_INVALID_ARG;
+    if (R > 0 && (!h || !hq || !hds)) return MOE_ERR_INVALID_ARG;
+    if (!al(h, 16) || !al(hq, 16) || !al(hds, d2s6 ? 8 : 4)) return MOE_ERR_ALIGNMENT;
+    if (R == 0) return MOE_OK;
+    return launch_requant_hidden(h, R, f, hq, hds, d2s6, S(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_quantize_scatter_q8_1(const float* x, int T, int d, int K, const int32_t* slot, int R,
+                              int8_t* q, uint16_t* ds, void* stream) {
+    return quantize_scatter(x, T, d, K, slot, R, q, ds, false, stream);
+}
+
+int moe_quantize_scatter_q8_1_d2s6(const float* x, int T, int d, int K, const int32_t* slot,
+                                   int R, int8_t* q, uint16_t* ds, void* stream) {
+    return quantize_scatter(x, T, d, K, slot, R, q, ds, true, stream);
 }
 
 int moe_quantize_gather_q8_1(const float* x, int T, int d, const int32_t* src, int R, int8_t* q,
                              uint16_t* ds, void* stream) {
-    if (T < 0 || R < 0 || d <= 0 || d % QK) return MOE_ERR_INVALID_ARG;
-    if (R > 0 && (!x || !src || !q || !ds)) return MOE_ERR_INVALID_ARG;
-    if (!al(x, 16) || !al(q, 16) || !al(ds, 4)) return MOE_ERR_ALIGNMENT;
-    if (R == 0) return MOE_OK;
-    return launch_quantize_gather(x, T, d, src, R, q, ds, S(stream));
+    return quantize_gather(x, T, d, src, R, q, ds, false, stream);
+}
+
+int moe_quantize_gather_q8_1_d2s6(const float* x, int T, int d, const int32_t* src, int R,
+                                  int8_t* q, uint16_t* ds, void* stream) {
+    return quantize_gather(x, T, d, src, R, q, ds, true, stream);
 }
 
 int moe_group_gather(const uint8_t* arena, size_t rec_bytes, size_t arena_stride,
@@ -210,11 +254,12 @@ int moe_grouped_mmq_gateup_q8_1(int wtype, const uint8_t* group_base, size_t slo
 
 int moe_requant_hidden_q8_1(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
                             void* stream) {
-    if (R < 0 || f <= 0 || f % QK) return MOE_ERR_INVALID_ARG;
-    if (R > 0 && (!h || !hq || !hds)) return MOE_ERR_INVALID_ARG;
-    if (!al(h, 16) || !al(hq, 16) || !al(hds, 4)) return MOE_ERR_ALIGNMENT;
-    if (R == 0) return MOE_OK;
-    return launch_requant_hidden(h, R, f, hq, hds, S(stream));
+    return requant_hidden(h, R, f, hq, hds, false, stream);
+}
+
+int moe_requant_hidden_q8_1_d2s6(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
+                                 void* stream) {
+    return requant_hidden(h, R, f, hq, hds, true, stream);
 }
 
 int moe_grouped_mmq_down(int wtype, const uint8_t* group_base, size_t slot_stride,

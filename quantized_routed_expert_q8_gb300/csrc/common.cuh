@@ -11,31 +11,39 @@
 
 namespace moe {
 
-constexpr int QK = 32;  // block width of q8_1, Q8_0, Q4_1 and Q2_0
+constexpr int QK = 32;    // block width of q8_1, Q8_0, Q4_1 and Q2_0
+constexpr int QKK = 256;  // Q2_K super-block width (sixteen 16-weight sub-blocks)
 
 // quant bytes per row of a weight matrix with reduction length k
 __host__ __device__ inline size_t quant_row_bytes(int wtype, int k) {
-    return (size_t)k / (wtype == MOE_W_Q4_1 ? 2 : wtype == MOE_W_Q2_0 ? 4 : 1);
+    return (size_t)k / (wtype == MOE_W_Q4_1 ? 2 : (wtype == MOE_W_Q2_0 || wtype == MOE_W_Q2_K) ? 4 : 1);
 }
+
+// binary16 entries per 32-block of a q8_1 ds row: (d, s), or (d, s, s_lo, s_hi)
+// in the D2S6 layout that Q2_K weights read
+__host__ __device__ inline int ds_halves(int wtype) { return wtype == MOE_W_Q2_K ? 4 : 2; }
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // One weight matrix of an expert record: quant plane [rows][K] (Q4_1: two
 // values per byte), fp16 d plane [K/32][rows] (block-major, so one block's
 // scales for consecutive rows are contiguous), fp16 m plane [K/32][rows] for
-// Q4_1 -- each plane 128-byte aligned.
+// Q4_1 -- each plane 128-byte aligned.  Q2_K: fp16 d and dmin (the m plane)
+// [K/256][rows], then the sub-block bytes sc | mn << 4 [K/16][rows] (plane s).
 struct MatLayout {
-    size_t q, d, m, bytes;
+    size_t q, d, m, s, bytes;
 };
 
 __host__ __device__ inline MatLayout mat_layout(int wtype, int rows, int k) {
     MatLayout L;
     size_t qb = (size_t)rows * quant_row_bytes(wtype, k);
-    size_t sb = (size_t)rows * (size_t)(k / QK) * 2;
+    size_t sb = (size_t)rows * (size_t)(k / (wtype == MOE_W_Q2_K ? QKK : QK)) * 2;
+    const bool has_m = wtype == MOE_W_Q4_1 || wtype == MOE_W_Q2_K;
     L.q = 0;
     L.d = align_up(qb, 128);
     L.m = L.d + align_up(sb, 128);
-    L.bytes = L.m + (wtype == MOE_W_Q4_1 ? align_up(sb, 128) : 0);
+    L.s = L.m + (has_m ? align_up(sb, 128) : 0);
+    L.bytes = L.s + (wtype == MOE_W_Q2_K ? align_up((size_t)rows * (size_t)(k / 16), 128) : 0);
     return L;
 }
 

@@ -5,7 +5,10 @@
 // For the expert at active position p and each of its rows r:
 //   acc = sum over 32-blocks b ascending of
 //         fma(fp32(dW[j,b]) * fp32(dx[r,b]), I_b, acc)  (+ fma(mW[j,b], sx[r,b], acc) for Q4_1)
-// (Q2_0: the block dot uses the weight integers c - 2)
+// (Q2_0: the block dot uses the weight integers c - 2.  Q2_K: the integers
+// sc * c with the sub-block scales of the block's two halves, dW the
+// super-block d, then fma(-(dmin * mn_lo), s_lo, acc) and fma(-(dmin * mn_hi),
+// s_hi, acc) from the D2S6 activation entries)
 // with I_b the exact int32 block dot -- the same fp32 operation sequence as the
 // scalar definition, so the result does not depend on the tiling.
 // Tile: 64 rows x 64 output columns per block of 256 threads, one 32-block of
@@ -23,22 +26,45 @@ __device__ __forceinline__ void unpack_q4_pair(uint32_t bytes2, uint32_t& w) {
     w = (b0 & 0xf) | ((b0 >> 4) << 8) | ((b1 & 0xf) << 16) | ((b1 >> 4) << 24);
 }
 
-// one Q2_0 byte (codes of 4 consecutive elements, 2 bits each) -> 4 int8 c - 2
-__device__ __forceinline__ int unpack_q2_byte(uint32_t x) {
-    const uint32_t spread = (x & 0x3u) | ((x & 0xCu) << 6) | ((x & 0x30u) << 12) | ((x & 0xC0u) << 18);
-    return (int)__vsub4(spread, 0x02020202u);
+// one byte of 2-bit codes (4 consecutive elements) -> 4 bytes c in 0..3
+__device__ __forceinline__ uint32_t spread_q2_byte(uint32_t x) {
+    return (x & 0x3u) | ((x & 0xCu) << 6) | ((x & 0x30u) << 12) | ((x & 0xC0u) << 18);
 }
 
+// one Q2_0 byte -> 4 int8 c - 2
+__device__ __forceinline__ int unpack_q2_byte(uint32_t x) {
+    return (int)__vsub4(spread_q2_byte(x), 0x02020202u);
+}
+
+// mw: [2][SB_N] -- the m term of each row (Q4_1: m; Q2_K: -(dmin * mn) of the
+// block's two halves)
 template <int WT>
 __device__ __forceinline__ void load_w_tile(const uint8_t* __restrict__ qplane,
                                             const __half* __restrict__ dplane,
-                                            const __half* __restrict__ mplane, int k, int j0,
+                                            const __half* __restrict__ mplane,
+                                            const uint8_t* __restrict__ splane, int k, int j0,
                                             int nrows, int b, int (*ws)[9], float* dw, float* mw,
                                             int tid) {
     // 64 weight rows x 32 values of block b
     if (tid < SB_N) {
         int j = j0 + tid;
-        if (j < nrows) {
+        if (j < nrows && WT == MOE_W_Q2_K) {
+            // codes times the sub-block scale: at most 3 * 15 per byte, so the
+            // 32-bit multiply of four spread bytes carries nothing across bytes
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(qplane + (size_t)j * (k / 4) + b * 8));
+            const uint32_t in[2] = {v.x, v.y};
+            const int u = b / (QKK / QK);
+            const float dmin = __half2float(mplane[(size_t)u * nrows + j]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t scmn = splane[(size_t)(2 * b + h) * nrows + j];
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    ws[tid][4 * h + t] = (int)(spread_q2_byte((in[h] >> (8 * t)) & 0xffu) * (scmn & 0xFu));
+                mw[h * SB_N + tid] = -__fmul_rn(dmin, (float)(scmn >> 4));
+            }
+            dw[tid] = __half2float(dplane[(size_t)u * nrows + j]);
+        } else if (j < nrows) {
             if (WT == MOE_W_Q8_0) {
                 const uint4* p = reinterpret_cast<const uint4*>(qplane + (size_t)j * k + b * QK);
                 uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
@@ -71,6 +97,7 @@ __device__ __forceinline__ void load_w_tile(const uint8_t* __restrict__ qplane,
             for (int w = 0; w < 8; ++w) ws[tid][w] = 0;
             dw[tid] = 0.0f;
             mw[tid] = 0.0f;
+            mw[SB_N + tid] = 0.0f;
         }
     }
 }
@@ -84,7 +111,8 @@ __global__ void __launch_bounds__(256) mmq_simt_kernel(
     __shared__ int xs[SB_M][9];
     __shared__ int wa[SB_N][9];
     __shared__ int wb[GATEUP ? SB_N : 1][9];
-    __shared__ float dx[SB_M], sx[SB_M], da[SB_N], ma[SB_N], db[SB_N], mb[SB_N];
+    // sx: s (Q4_1) or s_lo, s_hi (Q2_K) per row; ma / mb: the m terms per column
+    __shared__ float dx[SB_M], sx[2][SB_M], da[SB_N], ma[2][SB_N], db[SB_N], mb[2][SB_N];
     const int tile = blockIdx.y;
     if (tile >= *n_tiles) return;
     const int4 tl = tiles[tile];
@@ -98,6 +126,8 @@ __global__ void __launch_bounds__(256) mmq_simt_kernel(
     const __half* Am = reinterpret_cast<const __half*>(A + L.m);
     const __half* Bd = reinterpret_cast<const __half*>(B + L.d);
     const __half* Bm = reinterpret_cast<const __half*>(B + L.m);
+    const uint8_t* As = A + L.s;
+    const uint8_t* Bs = B + L.s;
     float acc_a[4][4], acc_b[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -117,16 +147,25 @@ __global__ void __launch_bounds__(256) mmq_simt_kernel(
             xs[row][half * 4 + 3] = v.w;
         } else if (tid < 192) {
             int row = tid - 128;
-            float2 f = make_float2(0.f, 0.f);
-            if (row < rows) f = __half22float2(xds[(size_t)(r0 + row) * nb + b]);
+            float2 f = make_float2(0.f, 0.f), g = make_float2(0.f, 0.f);
+            if (row < rows) {
+                if (WT == MOE_W_Q2_K) {  // D2S6: (d, s, s_lo, s_hi)
+                    const size_t e = ((size_t)(r0 + row) * nb + b) * 2;
+                    f = __half22float2(xds[e]);
+                    g = __half22float2(xds[e + 1]);
+                } else {
+                    f = __half22float2(xds[(size_t)(r0 + row) * nb + b]);
+                }
+            }
             dx[row] = f.x;
-            sx[row] = f.y;
+            sx[0][row] = WT == MOE_W_Q2_K ? g.x : f.y;
+            sx[1][row] = g.y;
         }
         if (tid >= 192) {
-            load_w_tile<WT>(A, Ad, Am, k, j0, n, b, wa, da, ma, tid - 192);
+            load_w_tile<WT>(A, Ad, Am, As, k, j0, n, b, wa, da, &ma[0][0], tid - 192);
         }
         if (GATEUP && tid < 64) {
-            load_w_tile<WT>(B, Bd, Bm, k, j0, n, b, wb, db, mb, tid);
+            load_w_tile<WT>(B, Bd, Bm, Bs, k, j0, n, b, wb, db, &mb[0][0], tid);
         }
         __syncthreads();
 #pragma unroll
@@ -149,10 +188,15 @@ __global__ void __launch_bounds__(256) mmq_simt_kernel(
                     if (GATEUP) Ib = __dp4a(xv, wvb[w], Ib);
                 }
                 acc_a[i][jj] = __fmaf_rn(__fmul_rn(da[col], dx[row]), (float)Ia, acc_a[i][jj]);
-                if (WT == MOE_W_Q4_1) acc_a[i][jj] = __fmaf_rn(ma[col], sx[row], acc_a[i][jj]);
+                if (WT == MOE_W_Q4_1 || WT == MOE_W_Q2_K)
+                    acc_a[i][jj] = __fmaf_rn(ma[0][col], sx[0][row], acc_a[i][jj]);
+                if (WT == MOE_W_Q2_K) acc_a[i][jj] = __fmaf_rn(ma[1][col], sx[1][row], acc_a[i][jj]);
                 if (GATEUP) {
                     acc_b[i][jj] = __fmaf_rn(__fmul_rn(db[col], dx[row]), (float)Ib, acc_b[i][jj]);
-                    if (WT == MOE_W_Q4_1) acc_b[i][jj] = __fmaf_rn(mb[col], sx[row], acc_b[i][jj]);
+                    if (WT == MOE_W_Q4_1 || WT == MOE_W_Q2_K)
+                        acc_b[i][jj] = __fmaf_rn(mb[0][col], sx[0][row], acc_b[i][jj]);
+                    if (WT == MOE_W_Q2_K)
+                        acc_b[i][jj] = __fmaf_rn(mb[1][col], sx[1][row], acc_b[i][jj]);
                 }
             }
         }
@@ -200,6 +244,9 @@ int launch_mmq_simt(int wtype, bool gateup, const uint8_t* group_base, size_t sl
     } else if (wtype == MOE_W_Q2_0) {
         if (gateup) MOE_SIMT_LAUNCH(MOE_W_Q2_0, true);
         else MOE_SIMT_LAUNCH(MOE_W_Q2_0, false);
+    } else if (wtype == MOE_W_Q2_K) {
+        if (gateup) MOE_SIMT_LAUNCH(MOE_W_Q2_K, true);
+        else MOE_SIMT_LAUNCH(MOE_W_Q2_K, false);
     } else {
         if (gateup) MOE_SIMT_LAUNCH(MOE_W_Q4_1, true);
         else MOE_SIMT_LAUNCH(MOE_W_Q4_1, false);

@@ -78,26 +78,40 @@ static_assert(THREADS * LAUNCH_REGS <= 65536, "launch registers exceed the regis
 constexpr int F16_A = 2 * BM * 64;  // two 128-row matrices x 32 fp16
 constexpr int F16_B = BN * 64;
 constexpr int F16_SLOT = F16_A + F16_B;
-constexpr int SC_SLOT = (2 * BM * 2 + BN * 2) * 4;  // dW, mW [256]; dX, sX [128] (fp32)
 
 __host__ __device__ constexpr int cround(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int WT>
 struct Lay {
+    // Q2_K: a stage's 4 blocks are half of one 256-weight super-block (one d and
+    // one dmin per row) and 8 sub-blocks (one sc | mn << 4 byte each per row);
+    // its activations are D2S6 (d, s, s_lo, s_hi), 8 bytes a block
+    static constexpr bool QK2 = WT == MOE_W_Q2_K;
     // raw weight bytes per row per stage (KBS blocks)
-    static constexpr int WROW = WT == MOE_W_Q8_0 ? 128 : WT == MOE_W_Q2_0 ? 32 : 64;
+    static constexpr int WROW = WT == MOE_W_Q8_0 ? 128 : (WT == MOE_W_Q2_0 || QK2) ? 32 : 64;
     static constexpr int W_RAW = 2 * BM * WROW;
     static constexpr int X_RAW = BN * 128;
-    static constexpr int WS_RAW = 2 * KBS * BM * 2;
-    static constexpr int WM_RAW = WT == MOE_W_Q4_1 ? WS_RAW : 0;
-    static constexpr int XS_RAW = BN * KBS * 4;
+    static constexpr int WS_RAW = QK2 ? 2 * BM * 2 : 2 * KBS * BM * 2;
+    static constexpr int WM_RAW = WT == MOE_W_Q4_1 ? WS_RAW : QK2 ? 2 * BM * 2 : 0;
+    static constexpr int WC_RAW = QK2 ? 2 * KBS * 2 * BM : 0;
+    static constexpr int XS_RAW = BN * KBS * (QK2 ? 8 : 4);
     static constexpr int O_W = 0;
     static constexpr int O_X = W_RAW;
     static constexpr int O_WS = O_X + X_RAW;
     static constexpr int O_WM = O_WS + WS_RAW;
-    static constexpr int O_XS = O_WM + WM_RAW;
+    static constexpr int O_WC = O_WM + WM_RAW;
+    static constexpr int O_XS = O_WC + WC_RAW;
     static constexpr int STAGE = cround(O_XS + XS_RAW, 1024);
-    static constexpr uint32_t TX = W_RAW + X_RAW + WS_RAW + WM_RAW + XS_RAW;
+    static constexpr uint32_t TX = W_RAW + X_RAW + WS_RAW + WM_RAW + WC_RAW + XS_RAW;
+    // fp32 scale slot (float offsets): dW [256], mW [256] (Q2_K: the first
+    // half's -dmin*mn, then the second half's [256]), dX [128], sX [128]
+    // (Q2_K: s_lo, then s_hi [128])
+    static constexpr int SC_MW = 2 * BM;
+    static constexpr int SC_MW2 = 4 * BM;
+    static constexpr int SC_DX = QK2 ? 6 * BM : 4 * BM;
+    static constexpr int SC_SX = SC_DX + BN;
+    static constexpr int SC_SX2 = SC_SX + BN;
+    static constexpr int SC_SLOT = (SC_SX + BN + (QK2 ? BN : 0)) * 4;
     static constexpr int O_F16 = RS * STAGE;
     static constexpr int O_SC = O_F16 + NFS * F16_SLOT;
     static constexpr int O_BAR = O_SC + NSC * SC_SLOT;
@@ -114,7 +128,10 @@ struct Lay {
 // hidden-row re-quantization of "#1368 ...", intro, done in the gate/up
 // epilogue): the stand-alone quantizer's operations, d = amax/127 and
 // q = round-half-away(v/d) with IEEE division, s = d * sum(q), so the bytes are
-// identical.  Token n0 + i is stored if it is below `rows`; lane 0 stores (d, s).
+// identical.  Token n0 + i is stored if it is below `rows`; lane 0 stores (d, s),
+// or with D2S6 (d, s, s_lo, s_hi) -- s_lo from lanes 0-15, s_hi from 16-31 --
+// as one 8-byte store (ds_stride then counts 8-byte entries).
+template <bool D2S6>
 __device__ __forceinline__ void requant16(const float (&v)[16], int n0, int rows, int8_t* q0,
                                           int q_stride, __half2* ds0, int ds_stride, int lane) {
     float amax[16];
@@ -139,18 +156,41 @@ __device__ __forceinline__ void requant16(const float (&v)[16], int n0, int rows
     int sum[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) sum[i] = qi[i];
+    // sums over each 16-lane half first (the D2S6 half sums), then the block
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1)
+    for (int o = 1; o <= 8; o <<= 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], o);
+    int hi[16];
+    if (D2S6) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) hi[i] = __shfl_sync(0xffffffffu, sum[i], 16);
+    }
+    int lo[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        lo[i] = sum[i];
+        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 16);
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const int n = n0 + i;
         if (n < rows) {
             q0[(size_t)n * q_stride] = (int8_t)qi[i];
-            if (lane == 0)
-                ds0[(size_t)n * ds_stride] =
+            if (lane == 0) {
+                const __half2 ds =
                     __halves2half2(__float2half_rn(d[i]), __float2half_rn(__fmul_rn(d[i], (float)sum[i])));
+                if (D2S6) {
+                    const __half2 lh = __halves2half2(__float2half_rn(__fmul_rn(d[i], (float)lo[i])),
+                                                      __float2half_rn(__fmul_rn(d[i], (float)hi[i])));
+                    uint2 e;
+                    e.x = *reinterpret_cast<const uint32_t*>(&ds);
+                    e.y = *reinterpret_cast<const uint32_t*>(&lh);
+                    reinterpret_cast<uint2*>(ds0)[(size_t)n * ds_stride] = e;
+                } else {
+                    ds0[(size_t)n * ds_stride] = ds;
+                }
+            }
         }
     }
 }
@@ -166,7 +206,7 @@ struct Params {
     uint32_t* err;
     // gate/up: q8_1 hidden rows written by the epilogue instead of h
     int8_t* hq;    // [R][f]
-    __half2* hds;  // [R][f/32] (d, s)
+    __half2* hds;  // [R][f/32] (d, s); Q2_K: [R][f/32] 8-byte (d, s, s_lo, s_hi)
     // down: the top-k combine of every (token, 256-column block) whose rows are complete
     float* comb;            // [T][d]
     const int32_t* src;     // row -> token
@@ -198,8 +238,9 @@ __device__ __forceinline__ Item load_item(const Params& P, int it) {
 template <int WT, bool GU, bool FUSED>
 __global__ void __launch_bounds__(THREADS, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mWs,
-                  const __grid_constant__ CUtensorMap mWm, const __grid_constant__ CUtensorMap mX,
-                  const __grid_constant__ CUtensorMap mXs, const Params P) {
+                  const __grid_constant__ CUtensorMap mWm, const __grid_constant__ CUtensorMap mWc,
+                  const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mXs,
+                  const Params P) {
     using L = Lay<WT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -399,21 +440,29 @@ __global__ void __launch_bounds__(THREADS, 1)
             const Item I = item(i);
             const int nch = min(4, max(0, (I.ncols - h * 64) / 16));  // active 16-column chunks
             const uint32_t tbase = lanes + tb * 256 + h * 64;
-            const float* sc = (const float*)(smem + L::O_SC + ss * SC_SLOT);
+            const float* sc = (const float*)(smem + L::O_SC + ss * L::SC_SLOT);
+            constexpr bool HAS_M = WT == MOE_W_Q4_1 || L::QK2;
             const float dA = sc[m], dB = sc[BM + m];
-            const float mA = WT == MOE_W_Q4_1 ? sc[2 * BM + m] : 0.0f;
-            const float mB = WT == MOE_W_Q4_1 ? sc[3 * BM + m] : 0.0f;
+            const float mA = HAS_M ? sc[L::SC_MW + m] : 0.0f;
+            const float mB = HAS_M ? sc[L::SC_MW + BM + m] : 0.0f;
+            const float nA = L::QK2 ? sc[L::SC_MW2 + m] : 0.0f;
+            const float nB = L::QK2 ? sc[L::SC_MW2 + BM + m] : 0.0f;
             const uint64_t dA2 = pk2(__float_as_uint(dA), __float_as_uint(dA));
             const uint64_t dB2 = pk2(__float_as_uint(dB), __float_as_uint(dB));
             const uint64_t mA2 = pk2(__float_as_uint(mA), __float_as_uint(mA));
             const uint64_t mB2 = pk2(__float_as_uint(mB), __float_as_uint(mB));
+            const uint64_t nA2 = pk2(__float_as_uint(nA), __float_as_uint(nA));
+            const uint64_t nB2 = pk2(__float_as_uint(nB), __float_as_uint(nB));
             // token scales as 16-byte loads (two pairs each, the same address in
             // every lane); a chunk's loads are issued before the work that hides
             // their latency
-            const ulonglong2* dX4 = reinterpret_cast<const ulonglong2*>(sc + 4 * BM + h * 64);
-            const ulonglong2* sX4 = reinterpret_cast<const ulonglong2*>(sc + 4 * BM + BN + h * 64);
+            const ulonglong2* dX4 = reinterpret_cast<const ulonglong2*>(sc + L::SC_DX + h * 64);
+            const ulonglong2* sX4 = reinterpret_cast<const ulonglong2*>(sc + L::SC_SX + h * 64);
+            const ulonglong2* tX4 = reinterpret_cast<const ulonglong2*>(sc + L::SC_SX2 + h * 64);
+            // Q2_K adds the second half's min term: fma(mW2, s_hi, acc)
             auto scale = [&](int c, const uint32_t(&ra)[16], const uint32_t(&rb)[16],
-                             const ulonglong2(&dx)[4], const ulonglong2(&sx)[4]) {
+                             const ulonglong2(&dx)[4], const ulonglong2(&sx)[4],
+                             const ulonglong2(&tx)[4]) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint64_t pa = pk2(ra[2 * j], ra[2 * j + 1]);
@@ -421,33 +470,42 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint64_t d2 = (j & 1) ? dx[j >> 1].y : dx[j >> 1].x;
                     accA[c][j] = fma2u(mul2u(dA2, d2), pa, accA[c][j]);
                     accB[c][j] = fma2u(mul2u(dB2, d2), pb, accB[c][j]);
-                    if (WT == MOE_W_Q4_1) {
+                    if (HAS_M) {
                         const uint64_t s2 = (j & 1) ? sx[j >> 1].y : sx[j >> 1].x;
                         accA[c][j] = fma2u(mA2, s2, accA[c][j]);
                         accB[c][j] = fma2u(mB2, s2, accB[c][j]);
                     }
+                    if (L::QK2) {
+                        const uint64_t t2 = (j & 1) ? tx[j >> 1].y : tx[j >> 1].x;
+                        accA[c][j] = fma2u(nA2, t2, accA[c][j]);
+                        accB[c][j] = fma2u(nB2, t2, accB[c][j]);
+                    }
                 }
             };
-            auto scales = [&](int c, ulonglong2(&dx)[4], ulonglong2(&sx)[4]) {
+            auto scales = [&](int c, ulonglong2(&dx)[4], ulonglong2(&sx)[4], ulonglong2(&tx)[4]) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) dx[k] = dX4[c * 4 + k];
-                if (WT == MOE_W_Q4_1) {
+                if (HAS_M) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) sx[k] = sX4[c * 4 + k];
+                }
+                if (L::QK2) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) tx[k] = tX4[c * 4 + k];
                 }
             };
 #pragma unroll
             for (int c2 = 0; c2 < 4; c2 += 2) {
                 if (c2 >= nch) continue;
-                ulonglong2 dx[4], sx[4];
-                scales(c2, dx, sx);  // in flight during the TMEM round trip
+                ulonglong2 dx[4], sx[4], tx[4];
+                scales(c2, dx, sx, tx);  // in flight during the TMEM round trip
                 // chunks c2 and c2 + 1 of both matrices in one round trip
                 uint32_t r[4][16];
                 tmem_ld16x4_wait(tbase + c2 * 16, tbase + 128 + c2 * 16, r);
-                scale(c2, r[0], r[2], dx, sx);
+                scale(c2, r[0], r[2], dx, sx, tx);
                 if (c2 + 1 < nch) {
-                    scales(c2 + 1, dx, sx);
-                    scale(c2 + 1, r[1], r[3], dx, sx);
+                    scales(c2 + 1, dx, sx, tx);
+                    scale(c2 + 1, r[1], r[3], dx, sx, tx);
                 }
             }
             tc_fence_before();
@@ -476,10 +534,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                             accA[c][j] = accB[c][j] = 0ull;
                         }
                         const int n0 = h * 64 + c * 16;
+                        // ds entries of row r0, block kb: (d, s) pairs, or 8-byte D2S6 entries
+                        __half2* ds0 =
+                            L::QK2 ? reinterpret_cast<__half2*>(reinterpret_cast<uint2*>(P.hds) +
+                                                                (size_t)I.r0 * (P.n_out / QK) + kb)
+                                   : P.hds + (size_t)I.r0 * (P.n_out / QK) + kb;
                         if (n0 < I.rows)  // warp-uniform
-                            requant16(v, n0, I.rows, P.hq + (size_t)I.r0 * P.n_out + I.w0 + m,
-                                      P.n_out, P.hds + (size_t)I.r0 * (P.n_out / QK) + kb,
-                                      P.n_out / QK, lane);
+                            requant16<L::QK2>(v, n0, I.rows,
+                                              P.hq + (size_t)I.r0 * P.n_out + I.w0 + m, P.n_out,
+                                              ds0, P.n_out / QK, lane);
                     }
                 } else {
 #pragma unroll
@@ -544,7 +607,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint8_t* st = smem + sl * L::STAGE;
             uint8_t* fa = smem + L::O_F16 + fs * F16_SLOT;
             uint8_t* fbB = fa + F16_A;
-            float* sc = (float*)(smem + L::O_SC + ss * SC_SLOT);
+            float* sc = (float*)(smem + L::O_SC + ss * L::SC_SLOT);
             // Thread ct's units: weight rows R0 + 64 * rep (Q8_0: both 16-byte
             // halves split over lanes; Q4_1: one 16-byte row ct + 128 * rep) and
             // tokens R0, R0 + 64.  Lanes 0-7 take 8 consecutive rows, lanes 8-15
@@ -560,7 +623,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int rep = 0; rep < NW; ++rep) {
                 if (WT == MOE_W_Q8_0) {
                     wv[rep] = *(const uint4*)(st + L::O_W + (rep * 64 + R0) * 128 + ch * 16);
-                } else if (WT == MOE_W_Q2_0) {
+                } else if (WT == MOE_W_Q2_0 || L::QK2) {
                     // 2-bit rows are 8 bytes a block, unswizzled: thread ct loads row ct
                     const uint2 v2 = *(const uint2*)(st + L::O_W + (rep * 128 + ct) * 32 + blk * 8);
                     wv[rep] = make_uint4(v2.x, v2.y, 0u, 0u);
@@ -573,18 +636,38 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint4 xv[2];
             xv[0] = x0 ? *(const uint4*)(st + L::O_X + R0 * 128 + ch * 16) : make_uint4(0, 0, 0, 0);
             xv[1] = x1 ? *(const uint4*)(st + L::O_X + (R0 + 64) * 128 + ch * 16) : make_uint4(0, 0, 0, 0);
-            // scales of block blk: dW (and mW) of rows ct, ct + 128; dX, sX of token ct
-            const int si0 = GU ? (blk * BM + ct) : (blk * 2 * BM + ct);
-            const int si1 = GU ? ((KBS + blk) * BM + ct) : (blk * 2 * BM + 128 + ct);
+            // scales of block blk: dW (and mW) of rows ct, ct + 128; dX, sX of token ct.
+            // Q2_K: the stage's super-block d and dmin ([mat][row] for gate/up,
+            // [row] for down: rows ct and ct + 128 either way) and the sub-block
+            // bytes of the block's two halves ([mat][8][row] / [8][256 rows])
+            const int si0 = L::QK2 ? ct : GU ? (blk * BM + ct) : (blk * 2 * BM + ct);
+            const int si1 = L::QK2 ? 128 + ct : GU ? ((KBS + blk) * BM + ct) : (blk * 2 * BM + 128 + ct);
             const __half* ws = (const __half*)(st + L::O_WS);
             const __half dw0 = ws[si0], dw1 = ws[si1];
             __half mw0 = __ushort_as_half(0), mw1 = __ushort_as_half(0);
-            if (WT == MOE_W_Q4_1) {
+            if (WT == MOE_W_Q4_1 || L::QK2) {
                 const __half* wm = (const __half*)(st + L::O_WM);
                 mw0 = wm[si0];
                 mw1 = wm[si1];
             }
-            const __half2 xs = ((const __half2*)(st + L::O_XS))[ct * KBS + blk];
+            uint32_t scmn[2][2] = {{0u, 0u}, {0u, 0u}};  // [rep][half]
+            if (L::QK2) {
+                const uint8_t* wc = st + L::O_WC;
+#pragma unroll
+                for (int rep = 0; rep < 2; ++rep)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+                        scmn[rep][hf] = wc[GU ? (rep * 2 * KBS + 2 * blk + hf) * BM + ct
+                                              : (2 * blk + hf) * 2 * BM + rep * 128 + ct];
+            }
+            uint2 xs2;  // (d, s) and, for D2S6, (s_lo, s_hi)
+            if (L::QK2) {
+                xs2 = ((const uint2*)(st + L::O_XS))[ct * KBS + blk];
+            } else {
+                xs2.x = ((const uint32_t*)(st + L::O_XS))[ct * KBS + blk];
+                xs2.y = 0u;
+            }
+            const __half2 xs = *reinterpret_cast<const __half2*>(&xs2.x);
             // weights: 256 rows x 32 values of block blk
 #pragma unroll
             for (int rep = 0; rep < NW; ++rep) {
@@ -598,14 +681,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint8_t* dst = fa + (R >> 7) * (BM * 64);
                     *(uint4*)(dst + f16_off(R & 127, 2 * hh)) = o0;
                     *(uint4*)(dst + f16_off(R & 127, 2 * hh + 1)) = o1;
-                } else if (WT == MOE_W_Q2_0) {
+                } else if (WT == MOE_W_Q2_0 || L::QK2) {
                     const int R = rep * 128 + ct;
                     const uint32_t w2[2] = {wv[rep].x, wv[rep].y};
                     uint8_t* dst = fa + (R >> 7) * (BM * 64);
 #pragma unroll
                     for (int c2 = 0; c2 < 2; ++c2) {  // elements 16*c2 .. 16*c2 + 15
                         uint32_t a[4], b[4];
-                        cvt_u2x16(w2[c2], a, b);
+                        if (L::QK2)  // Q2_K: c * sc of the half's sub-block
+                            cvt_u2x16_scaled(w2[c2], scmn[rep][c2] & 0xFu, a, b);
+                        else
+                            cvt_u2x16(w2[c2], a, b);
                         *(uint4*)(dst + f16_off(R & 127, 2 * c2)) = make_uint4(a[0], a[1], a[2], a[3]);
                         *(uint4*)(dst + f16_off(R & 127, 2 * c2 + 1)) = make_uint4(b[0], b[1], b[2], b[3]);
                     }
@@ -643,15 +729,29 @@ __global__ void __launch_bounds__(THREADS, 1)
                     *(uint4*)(fbB + f16_off(n, 2 * hh + 1)) = o1;
                 }
             }
-            // scales as fp32: dW[256], mW[256], dX[128], sX[128]
+            // scales as fp32: dW[256], mW[256] (Q2_K: -dmin*mn of each half, exact
+            // products), dX[128], sX[128] (Q2_K: s_lo, s_hi)
             sc[ct] = __half2float(dw0);
             sc[128 + ct] = __half2float(dw1);
             if (WT == MOE_W_Q4_1) {
-                sc[2 * BM + ct] = __half2float(mw0);
-                sc[2 * BM + 128 + ct] = __half2float(mw1);
+                sc[L::SC_MW + ct] = __half2float(mw0);
+                sc[L::SC_MW + 128 + ct] = __half2float(mw1);
             }
-            sc[4 * BM + ct] = __low2float(xs);
-            sc[4 * BM + BN + ct] = __high2float(xs);
+            if (L::QK2) {
+                const float dm[2] = {__half2float(mw0), __half2float(mw1)};
+#pragma unroll
+                for (int rep = 0; rep < 2; ++rep) {
+                    sc[L::SC_MW + rep * 128 + ct] = -__fmul_rn(dm[rep], (float)(scmn[rep][0] >> 4));
+                    sc[L::SC_MW2 + rep * 128 + ct] = -__fmul_rn(dm[rep], (float)(scmn[rep][1] >> 4));
+                }
+                const __half2 lh = *reinterpret_cast<const __half2*>(&xs2.y);
+                sc[L::SC_DX + ct] = __low2float(xs);
+                sc[L::SC_SX + ct] = __low2float(lh);
+                sc[L::SC_SX2 + ct] = __high2float(lh);
+            } else {
+                sc[L::SC_DX + ct] = __low2float(xs);
+                sc[L::SC_SX + ct] = __high2float(xs);
+            }
             // make this thread's fp16 operands visible to the tensor core, then one
             // arrival per warp and barrier
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -680,17 +780,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t st = sbase + sl * L::STAGE;
                 const uint32_t fb = bar(B_RAW_FULL + sl);
                 mbar_expect_tx(fb, L::TX);
+                // scale-plane coordinate of the stage: its first block, or for
+                // Q2_K its super-block (two stages each) and first sub-block
+                const int sy = L::QK2 ? s / 2 : s * KBS;
                 if (GU) {
                     tma_4d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, 0, I.p);
-                    tma_4d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, 0, I.p);
-                    if (WT == MOE_W_Q4_1) tma_4d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, 0, I.p);
+                    tma_4d(&mWs, fb, st + L::O_WS, I.w0, sy, 0, I.p);
+                    if (L::WM_RAW) tma_4d(&mWm, fb, st + L::O_WM, I.w0, sy, 0, I.p);
+                    if (L::QK2) tma_4d(&mWc, fb, st + L::O_WC, I.w0, s * 2 * KBS, 0, I.p);
                 } else {
                     tma_3d(&mW, fb, st + L::O_W, s * L::WROW, I.w0, I.p);
-                    tma_3d(&mWs, fb, st + L::O_WS, I.w0, s * KBS, I.p);
-                    if (WT == MOE_W_Q4_1) tma_3d(&mWm, fb, st + L::O_WM, I.w0, s * KBS, I.p);
+                    tma_3d(&mWs, fb, st + L::O_WS, I.w0, sy, I.p);
+                    if (L::WM_RAW) tma_3d(&mWm, fb, st + L::O_WM, I.w0, sy, I.p);
+                    if (L::QK2) tma_3d(&mWc, fb, st + L::O_WC, I.w0, s * 2 * KBS, I.p);
                 }
                 tma_2d(&mX, fb, st + L::O_X, s * 128, I.r0);
-                tma_2d(&mXs, fb, st + L::O_XS, s * KBS, I.r0);
+                // activation scales: 4-byte (d, s), or 8-byte D2S6 entries as two words
+                tma_2d(&mXs, fb, st + L::O_XS, s * KBS * (L::QK2 ? 2 : 1), I.r0);
             }
             // drain the copies still in flight before the CTA may exit (waits
             // only on the abort path)
@@ -862,7 +968,11 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     const CUtensorMapSwizzle wsw = WT == MOE_W_Q8_0   ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : WT == MOE_W_Q4_1 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                       : CU_TENSOR_MAP_SWIZZLE_NONE;
-    CUtensorMap mW, mWs, mWm, mX, mXs;
+    // scale planes: per 32-block [K/32][rows], or Q2_K's per super-block
+    // [K/256][rows] (d, dmin) with one stage loading one super-block row
+    const uint64_t n_sb = (uint64_t)(K / (L::QK2 ? QKK : QK));
+    const uint32_t sbox = L::QK2 ? 1u : (uint32_t)KBS;
+    CUtensorMap mW, mWs, mWm, mWc, mX, mXs;
     bool ok = true;
     if (GU) {
         uint64_t dq[4] = {wrow, (uint64_t)rows, 2, S};
@@ -870,28 +980,46 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
         uint32_t bq[4] = {(uint32_t)L::WROW, BM, 2, 1};
         ok &= make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, mbase + ML.q, dq, sq, bq,
                        wsw, "W (gate/up)");
-        uint64_t ds[4] = {(uint64_t)rows, (uint64_t)(K / QK), 2, S};
+        uint64_t ds[4] = {(uint64_t)rows, n_sb, 2, S};
         uint64_t ss[3] = {(uint64_t)rows * 2, RL.gu.bytes, slot_stride};
-        uint32_t bs[4] = {BM, KBS, 2, 1};
+        uint32_t bs[4] = {BM, sbox, 2, 1};
         ok &= make_map(&mWs, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, mbase + ML.d, ds, ss, bs,
                        CU_TENSOR_MAP_SWIZZLE_NONE, "W scales (gate/up)");
         ok &= make_map(&mWm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
-                       mbase + (WT == MOE_W_Q4_1 ? ML.m : ML.d), ds, ss, bs,
+                       mbase + (L::WM_RAW ? ML.m : ML.d), ds, ss, bs,
                        CU_TENSOR_MAP_SWIZZLE_NONE, "W mins (gate/up)");
+        if (L::QK2) {
+            uint64_t dc[4] = {(uint64_t)rows, (uint64_t)(K / 16), 2, S};
+            uint64_t sc[3] = {(uint64_t)rows, RL.gu.bytes, slot_stride};
+            uint32_t bc[4] = {BM, 2 * KBS, 2, 1};
+            ok &= make_map(&mWc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, mbase + ML.s, dc, sc, bc,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, "W sub-block scales (gate/up)");
+        } else {
+            mWc = mWs;  // unused
+        }
     } else {
         uint64_t dq[3] = {wrow, (uint64_t)rows, S};
         uint64_t sq[2] = {wrow, slot_stride};
         uint32_t bq[3] = {(uint32_t)L::WROW, 2 * BM, 1};
         ok &= make_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, mbase + ML.q, dq, sq, bq,
                        wsw, "W (down)");
-        uint64_t ds[3] = {(uint64_t)rows, (uint64_t)(K / QK), S};
+        uint64_t ds[3] = {(uint64_t)rows, n_sb, S};
         uint64_t ss[2] = {(uint64_t)rows * 2, slot_stride};
-        uint32_t bs[3] = {2 * BM, KBS, 1};
+        uint32_t bs[3] = {2 * BM, sbox, 1};
         ok &= make_map(&mWs, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, mbase + ML.d, ds, ss, bs,
                        CU_TENSOR_MAP_SWIZZLE_NONE, "W scales (down)");
         ok &= make_map(&mWm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
-                       mbase + (WT == MOE_W_Q4_1 ? ML.m : ML.d), ds, ss, bs,
+                       mbase + (L::WM_RAW ? ML.m : ML.d), ds, ss, bs,
                        CU_TENSOR_MAP_SWIZZLE_NONE, "W mins (down)");
+        if (L::QK2) {
+            uint64_t dc[3] = {(uint64_t)rows, (uint64_t)(K / 16), S};
+            uint64_t sc[2] = {(uint64_t)rows, slot_stride};
+            uint32_t bc[3] = {2 * BM, 2 * KBS, 1};
+            ok &= make_map(&mWc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, mbase + ML.s, dc, sc, bc,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, "W sub-block scales (down)");
+        } else {
+            mWc = mWs;  // unused
+        }
     }
     {
         uint64_t dx[2] = {(uint64_t)K, (uint64_t)R};
@@ -899,9 +1027,11 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
         uint32_t bx[2] = {128, BN};
         ok &= make_map(&mX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, xq, dx, sx, bx,
                        CU_TENSOR_MAP_SWIZZLE_128B, "X");
-        uint64_t dd[2] = {(uint64_t)(K / QK), (uint64_t)R};
-        uint64_t sd[1] = {(uint64_t)(K / QK) * 4};
-        uint32_t bd[2] = {KBS, BN};
+        // (d, s) as one word per block, or D2S6's 8 bytes as two words
+        const uint64_t wpb = L::QK2 ? 2 : 1;
+        uint64_t dd[2] = {(uint64_t)(K / QK) * wpb, (uint64_t)R};
+        uint64_t sd[1] = {(uint64_t)(K / QK) * 4 * wpb};
+        uint32_t bd[2] = {(uint32_t)(KBS * wpb), BN};
         ok &= make_map(&mXs, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, xds, dd, sd, bd,
                        CU_TENSOR_MAP_SWIZZLE_NONE, "X scales");
     }
@@ -930,7 +1060,7 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     P.T = F.T;
     long long upper = ((long long)R / BN + E + 1) * P.mt_count;
     int grid = (int)(upper < sms ? upper : sms);
-    mmq_tc_kernel<WT, GU, FUSED><<<grid, THREADS, L::SMEM, stream>>>(mW, mWs, mWm, mX, mXs, P);
+    mmq_tc_kernel<WT, GU, FUSED><<<grid, THREADS, L::SMEM, stream>>>(mW, mWs, mWm, mWc, mX, mXs, P);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess && debug())
@@ -942,13 +1072,17 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
 }  // namespace tc
 
 bool mmq_tc_supported(int wtype, bool gateup, int d, int f) {
-    if (wtype != MOE_W_Q8_0 && wtype != MOE_W_Q4_1 && wtype != MOE_W_Q2_0) return false;
+    if (wtype != MOE_W_Q8_0 && wtype != MOE_W_Q4_1 && wtype != MOE_W_Q2_0 && wtype != MOE_W_Q2_K)
+        return false;
     if (d % 256 || f % 128) return false;  // whole 128-row weight tiles, 128-wide K stages
+    if (wtype == MOE_W_Q2_K && f % 256) return false;  // whole super-blocks of the down reduction
     if (tc::encode_fn() == nullptr) return false;
     if (wtype == MOE_W_Q8_0)
         return gateup ? tc::kernel_ready<MOE_W_Q8_0, true>() : tc::kernel_ready<MOE_W_Q8_0, false>();
     if (wtype == MOE_W_Q2_0)
         return gateup ? tc::kernel_ready<MOE_W_Q2_0, true>() : tc::kernel_ready<MOE_W_Q2_0, false>();
+    if (wtype == MOE_W_Q2_K)
+        return gateup ? tc::kernel_ready<MOE_W_Q2_K, true>() : tc::kernel_ready<MOE_W_Q2_K, false>();
     return gateup ? tc::kernel_ready<MOE_W_Q4_1, true>() : tc::kernel_ready<MOE_W_Q4_1, false>();
 }
 
@@ -981,6 +1115,9 @@ int launch_mmq_tc(int wtype, bool gateup, const uint8_t* group_base, size_t slot
                                          ws, W, F, stream);
     if (wtype == MOE_W_Q2_0)
         return tc::launch_wt<MOE_W_Q2_0>(gateup, group_base, slot_stride, E, xq, xds, R, d, f, out,
+                                         ws, W, F, stream);
+    if (wtype == MOE_W_Q2_K)
+        return tc::launch_wt<MOE_W_Q2_K>(gateup, group_base, slot_stride, E, xq, xds, R, d, f, out,
                                          ws, W, F, stream);
     return tc::launch_wt<MOE_W_Q4_1>(gateup, group_base, slot_stride, E, xq, xds, R, d, f, out, ws,
                                      W, F, stream);

@@ -11,11 +11,17 @@
 // single rounding (__fmul_rn), and nothing is flushed to zero, so the bytes
 // match any correct implementation of the definition.
 //
+// D2S6 layout (the rows Q2_K weights read; the pages name it without defining
+// it): the same q and (d, s), followed per block by (s_lo, s_hi) = fp16 of d
+// times the sums of q over the block's two 16-value halves.
+//
 // Mapping: one thread per 16 consecutive values (four 16-byte loads), two
 // threads per 32-block, amax and sum(q) reduced with one xor shuffle each.  A
 // warp covers 512 consecutive values of a row: each thread stores its 16 quants
 // as one 16-byte store, so a warp's q stores are 512 contiguous bytes per
-// destination row and its (d, s) stores 64 contiguous bytes.
+// destination row and its (d, s) stores 64 contiguous bytes (128 for D2S6).
+// The thread of the first half of a block holds the sum of its own 16 quants,
+// which is s_lo, and receives s_hi's sum from the shuffle.
 #include "common.cuh"
 
 namespace moe {
@@ -25,8 +31,10 @@ enum QuantMode { QUANT_SCATTER = 0, QUANT_GATHER = 1, QUANT_IDENTITY = 2 };
 struct Q8Half {
     uint4 q;      // 16 int8 quants
     __half2 ds;   // (d, s), valid in both lanes of the pair
+    __half2 lh;   // D2S6 (s_lo, s_hi), valid in the first-half lane
 };
 
+template <bool D2S6>
 __device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
     float v[16];
 #pragma unroll
@@ -77,15 +85,31 @@ __device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
             w[i >> 2] |= (uint32_t)(qi & 0xff) << (8 * (i & 3));
         }
     }
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    const float s = __fmul_rn(d, (float)sum);
+    const int other = __shfl_xor_sync(0xffffffffu, sum, 1);
+    const float s = __fmul_rn(d, (float)(sum + other));
     r.q = make_uint4(w[0], w[1], w[2], w[3]);
     r.ds = __halves2half2(__float2half_rn(d), __float2half_rn(s));
+    if (D2S6)
+        r.lh = __halves2half2(__float2half_rn(__fmul_rn(d, (float)sum)),
+                              __float2half_rn(__fmul_rn(d, (float)other)));
     return r;
 }
 
-// x: [n_src_rows][d]; writes rows of q [R][d] / ds [R][d/32].
-template <int MODE>
+// one block's ds entries: (d, s), or (d, s, s_lo, s_hi) as one 8-byte store
+template <bool D2S6>
+__device__ __forceinline__ void store_ds(__half2* ds, size_t blk, const Q8Half& b) {
+    if (D2S6) {
+        uint2 v;
+        v.x = *reinterpret_cast<const uint32_t*>(&b.ds);
+        v.y = *reinterpret_cast<const uint32_t*>(&b.lh);
+        reinterpret_cast<uint2*>(ds)[blk] = v;
+    } else {
+        ds[blk] = b.ds;
+    }
+}
+
+// x: [n_src_rows][d]; writes rows of q [R][d] / ds [R][d/32] (x2 for D2S6).
+template <int MODE, bool D2S6>
 __global__ void __launch_bounds__(256, 4) quantize_q8_1_kernel(
     const float* __restrict__ x, int n_src_rows, int d, int K, const int32_t* __restrict__ map,
     int R, int8_t* __restrict__ q, __half2* __restrict__ ds, long long n_units) {
@@ -112,7 +136,7 @@ __global__ void __launch_bounds__(256, 4) quantize_q8_1_kernel(
             for (int i = 0; i < 4; ++i)  // gather rows are re-read K times: keep them cached;
                 a[i] = MODE == QUANT_GATHER ? __ldg(p + i) : __ldcs(p + i);  // else stream past L2
         }
-        const Q8Half blk = quantize16(a);
+        const Q8Half blk = quantize16<D2S6>(a);
         if (!in) continue;
         const bool lead = (threadIdx.x & 1) == 0;
         if (MODE == QUANT_SCATTER) {
@@ -120,12 +144,12 @@ __global__ void __launch_bounds__(256, 4) quantize_q8_1_kernel(
                 const int r = map[row * K + k];
                 if ((unsigned)r >= (unsigned)R) continue;
                 *reinterpret_cast<uint4*>(q + (size_t)r * d + c) = blk.q;
-                if (lead) ds[(size_t)r * (d / QK) + c / QK] = blk.ds;
+                if (lead) store_ds<D2S6>(ds, (size_t)r * (d / QK) + c / QK, blk);
             }
         } else {
             if (row >= R) continue;
             *reinterpret_cast<uint4*>(q + (size_t)row * d + c) = blk.q;
-            if (lead) ds[(size_t)row * (d / QK) + c / QK] = blk.ds;
+            if (lead) store_ds<D2S6>(ds, (size_t)row * (d / QK) + c / QK, blk);
         }
     }
 }
@@ -140,31 +164,46 @@ static int quant_grid(long long n_units) {
 }
 
 int launch_quantize_scatter(const float* x, int T, int d, int K, const int32_t* slot, int R,
-                            int8_t* q, uint16_t* ds, cudaStream_t stream) {
+                            int8_t* q, uint16_t* ds, bool d2s6, cudaStream_t stream) {
     long long n = (long long)T * (d / 16);
     if (n == 0) return MOE_OK;
-    quantize_q8_1_kernel<QUANT_SCATTER><<<quant_grid(n), 256, 0, stream>>>(
-        x, T, d, K, slot, R, q, reinterpret_cast<__half2*>(ds), n);
+    __half2* ds2 = reinterpret_cast<__half2*>(ds);
+    if (d2s6)
+        quantize_q8_1_kernel<QUANT_SCATTER, true><<<quant_grid(n), 256, 0, stream>>>(
+            x, T, d, K, slot, R, q, ds2, n);
+    else
+        quantize_q8_1_kernel<QUANT_SCATTER, false><<<quant_grid(n), 256, 0, stream>>>(
+            x, T, d, K, slot, R, q, ds2, n);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int launch_quantize_gather(const float* x, int T, int d, const int32_t* src, int R, int8_t* q,
-                           uint16_t* ds, cudaStream_t stream) {
+                           uint16_t* ds, bool d2s6, cudaStream_t stream) {
     long long n = (long long)R * (d / 16);
     if (n == 0) return MOE_OK;
-    quantize_q8_1_kernel<QUANT_GATHER><<<quant_grid(n), 256, 0, stream>>>(
-        x, T, d, 1, src, R, q, reinterpret_cast<__half2*>(ds), n);
+    __half2* ds2 = reinterpret_cast<__half2*>(ds);
+    if (d2s6)
+        quantize_q8_1_kernel<QUANT_GATHER, true><<<quant_grid(n), 256, 0, stream>>>(
+            x, T, d, 1, src, R, q, ds2, n);
+    else
+        quantize_q8_1_kernel<QUANT_GATHER, false><<<quant_grid(n), 256, 0, stream>>>(
+            x, T, d, 1, src, R, q, ds2, n);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-int launch_requant_hidden(const float* h, int R, int f, int8_t* hq, uint16_t* hds,
+int launch_requant_hidden(const float* h, int R, int f, int8_t* hq, uint16_t* hds, bool d2s6,
                           cudaStream_t stream) {
     long long n = (long long)R * (f / 16);
     if (n == 0) return MOE_OK;
-    quantize_q8_1_kernel<QUANT_IDENTITY><<<quant_grid(n), 256, 0, stream>>>(
-        h, R, f, 1, nullptr, R, hq, reinterpret_cast<__half2*>(hds), n);
+    __half2* ds2 = reinterpret_cast<__half2*>(hds);
+    if (d2s6)
+        quantize_q8_1_kernel<QUANT_IDENTITY, true><<<quant_grid(n), 256, 0, stream>>>(
+            h, R, f, 1, nullptr, R, hq, ds2, n);
+    else
+        quantize_q8_1_kernel<QUANT_IDENTITY, false><<<quant_grid(n), 256, 0, stream>>>(
+            h, R, f, 1, nullptr, R, hq, ds2, n);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -86,7 +86,11 @@ extern "C" int moe_layer_forward_streamed(int wtype, int T, int K, int E, int d,
     rc = moe_build_slot_map(ids, T, K, E, b->offsets, b->slot, b->src, b->active, b->n_active,
                             b->ws, b->ws_bytes, compute_stream);
     if (rc != MOE_OK) return rc;
-    rc = moe_quantize_scatter_q8_1(x, T, d, K, b->slot, R, b->q, b->ds, compute_stream);
+    // Q2_K's MMQ reads the D2S6 layout (d, s, s_lo, s_hi); the others (d, s)
+    const bool d2s6 = wtype == MOE_W_Q2_K;
+    const int dsw = d2s6 ? 4 : 2;
+    rc = (d2s6 ? moe_quantize_scatter_q8_1_d2s6 : moe_quantize_scatter_q8_1)(
+        x, T, d, K, b->slot, R, b->q, b->ds, compute_stream);
     if (rc != MOE_OK) return rc;
 
     // the routed experts and their row ranges, on the host
@@ -152,9 +156,9 @@ extern "C" int moe_layer_forward_streamed(int wtype, int T, int K, int E, int d,
                                     b->ws, b->ws_bytes, compute_stream);
         if (rc != MOE_OK) return rc;
         if (r1 > r0) {
-            rc = moe_requant_hidden_q8_1(b->h + (size_t)r0 * f, r1 - r0, f,
-                                         b->hq + (size_t)r0 * f, b->hds + (size_t)r0 * (f / 32) * 2,
-                                         compute_stream);
+            rc = (d2s6 ? moe_requant_hidden_q8_1_d2s6 : moe_requant_hidden_q8_1)(
+                b->h + (size_t)r0 * f, r1 - r0, f, b->hq + (size_t)r0 * f,
+                b->hds + (size_t)r0 * (f / 32) * dsw, compute_stream);
             if (rc != MOE_OK) return rc;
         }
         rc = moe_grouped_mmq_down(wtype, b->group_buf, slot_stride, b->active + g * GROUP,

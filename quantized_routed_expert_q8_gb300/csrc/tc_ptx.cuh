@@ -284,6 +284,27 @@ __device__ __forceinline__ void cvt_u2x16(uint32_t w, uint32_t (&a)[4], uint32_t
     }
 }
 
+// As cvt_u2x16 for Q2_K: the 16 codes of one sub-block times its scale sc,
+// fp16 pairs of c * sc in the same order.  (1024 + c) * sc - 1024 * sc is one
+// fused operation whose exact value c * sc <= 45 is representable, so the
+// single rounding returns it exactly.
+__device__ __forceinline__ void cvt_u2x16_scaled(uint32_t w, uint32_t sc, uint32_t (&a)[4],
+                                                 uint32_t (&b)[4]) {
+    const __half hs = __uint2half_rn(sc);  // sc <= 15: exact
+    const __half2 m2 = __halves2half2(hs, hs);
+    const __half hb = __hneg(__hmul(__ushort_as_half((unsigned short)0x6400u), hs));  // -1024 * sc, exact
+    const __half2 b2 = __halves2half2(hb, hb);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t t = (w >> (2 * k)) & 0x03030303u;
+        uint32_t xa = prmt(t, MAGIC, 0x4140u), xb = prmt(t, MAGIC, 0x4342u);
+        __half2 ra = __hfma2(*reinterpret_cast<__half2*>(&xa), m2, b2);
+        __half2 rb = __hfma2(*reinterpret_cast<__half2*>(&xb), m2, b2);
+        a[k] = *reinterpret_cast<uint32_t*>(&ra);
+        b[k] = *reinterpret_cast<uint32_t*>(&rb);
+    }
+}
+
 // byte offset of (row, 16-byte chunk c) in the fp16 K-major operand layout:
 // [row/8][chunk 0..3][row%8][16 B]  (lbo = 128, sbo = 512)
 __device__ __forceinline__ uint32_t f16_off(int row, int c) {

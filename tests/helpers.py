@@ -93,41 +93,65 @@ def oracle_layer_tokens(wl: mw.Workload, toks) -> np.ndarray:
 # the CUDA library), shared by the oracle pins and the GPU tolerance bounds.
 
 def _qbytes(wtype, rows, k):
-    return rows * k // {mw.Q8_0: 1, mw.Q4_1: 2, mw.Q2_0: 4}[wtype]
+    return rows * k // {mw.Q8_0: 1, mw.Q4_1: 2, mw.Q2_0: 4, mw.Q2_K: 4}[wtype]
+
+
+def _a128(v):
+    return (v + 127) // 128 * 128
+
+
+def _codes2(p, rows, k):
+    """2-bit codes packed four per byte: element 4j+i in bits 2i..2i+1 of byte j."""
+    p = p.reshape(rows, k // 4).astype(np.int64)
+    c = np.empty((rows, k), np.int64)
+    for i in range(4):
+        c[:, i::4] = (p >> (2 * i)) & 3
+    return c
 
 
 def _planes(wtype, rec, off, rows, k):
-    """Decode one matrix of a record with numpy (independent of the oracle).
-    Q2_0 codes come back as their values c - 2."""
+    """Decode one matrix of a record with numpy (independent of the oracle) into
+    (q, dpl, mpl) with w = q * dpl + mpl, each scale plane repeated along k to
+    its block width.  Q2_0 codes come back as their values c - 2; Q2_K as
+    sc * c, with dpl the super-block d [rows, k/256] and mpl = -dmin * mn
+    [rows, k/16]."""
     qb = _qbytes(wtype, rows, k)
-    a128 = lambda v: (v + 127) // 128 * 128
-    sb = rows * (k // 32) * 2
     base = rec[off:]
+    if wtype == mw.Q2_K:
+        sb = rows * (k // 256) * 2
+        o = _a128(qb)
+        dpl = base[o:o + sb].view(np.float16).reshape(k // 256, rows).T.astype(np.float64)
+        o += _a128(sb)
+        dmin = base[o:o + sb].view(np.float16).reshape(k // 256, rows).T.astype(np.float64)
+        o += _a128(sb)
+        scmn = base[o:o + rows * (k // 16)].reshape(k // 16, rows).T.astype(np.int64)
+        q = _codes2(base[:qb], rows, k) * np.repeat(scmn & 0x0F, 16, axis=1)
+        mpl = -np.repeat(dmin, 16, axis=1) * (scmn >> 4)
+        return q, dpl, mpl
+    sb = rows * (k // 32) * 2
     if wtype == mw.Q8_0:
         q = base[:qb].view(np.int8).reshape(rows, k).astype(np.int64)
     elif wtype == mw.Q2_0:
-        p = base[:qb].reshape(rows, k // 4).astype(np.int64)
-        q = np.empty((rows, k), np.int64)
-        for i in range(4):  # element 4j+i sits in bits 2i..2i+1 of byte j
-            q[:, i::4] = ((p >> (2 * i)) & 3) - 2
+        q = _codes2(base[:qb], rows, k) - 2
     else:
         p = base[:qb].reshape(rows, k // 2)
         q = np.empty((rows, k), np.int64)
         q[:, 0::2] = p & 0x0F
         q[:, 1::2] = p >> 4
     # scale planes are block-major [k/32][rows]
-    dpl = base[a128(qb):a128(qb) + sb].view(np.float16).reshape(k // 32, rows).T.astype(np.float64)
+    dpl = base[_a128(qb):_a128(qb) + sb].view(np.float16).reshape(k // 32, rows).T.astype(np.float64)
     mpl = None
     if wtype == mw.Q4_1:
-        o = a128(qb) + a128(sb)
+        o = _a128(qb) + _a128(sb)
         mpl = base[o:o + sb].view(np.float16).reshape(k // 32, rows).T.astype(np.float64)
     return q, dpl, mpl
 
 
 def _dequant_w(q, dpl, mpl):
-    w = q.astype(np.float64) * np.repeat(dpl, 32, axis=1)
+    k = q.shape[1]
+    w = q.astype(np.float64) * np.repeat(dpl, k // dpl.shape[1], axis=1)
     if mpl is not None:
-        w += np.repeat(mpl, 32, axis=1)
+        w += np.repeat(mpl, k // mpl.shape[1], axis=1)
     return w
 
 
@@ -136,18 +160,27 @@ def _dequant_x(q, ds):
     return q.astype(np.float64) * np.repeat(dx, 32, axis=1)
 
 
+def _msums(wtype, ds):
+    """The activation sums the weight type's m term multiplies: s per 32-block
+    (Q4_1) or (s_lo, s_hi) per 32-block, i.e. one per 16 values (Q2_K)."""
+    if wtype == mw.Q2_K:
+        return ds[..., 2:4].reshape(ds.shape[0], -1).view(np.float16).astype(np.float64)
+    return ds[..., 1].view(np.float16).astype(np.float64)
+
+
 def _mat_offsets(wtype, d, f):
-    a128 = lambda v: (v + 127) // 128 * 128
     qb = _qbytes(wtype, f, d)
-    sb = f * (d // 32) * 2
-    g = a128(qb) + a128(sb) * (2 if wtype == mw.Q4_1 else 1)
+    if wtype == mw.Q2_K:
+        g = _a128(qb) + 2 * _a128(f * (d // 256) * 2) + _a128(f * (d // 16))
+    else:
+        sb = f * (d // 32) * 2
+        g = _a128(qb) + _a128(sb) * (2 if wtype == mw.Q4_1 else 1)
     return 0, g, 2 * g
 
 
-
-
 def abs_dot_bound(stage: str, wl: mw.Workload, offsets, xq, xds, rows) -> np.ndarray:
-    """sum over k of |w_k| * |x_k| (+ sum over blocks of |m| * |s| for Q4_1) for
+    """sum over k of |w_k| * |x_k| (+ sum of |m| * |s| over the m term's blocks,
+    Q4_1 and Q2_K) for
     every output of the listed rows, with the dequantized weights of each row's
     expert: the magnitude that bounds the rounding error of any summation order
     of one output of stage 'gateup' (gate rows then up rows) or 'down'."""
@@ -159,7 +192,7 @@ def abs_dot_bound(stage: str, wl: mw.Workload, offsets, xq, xds, rows) -> np.nda
     st = wl.arena_stride
     out = []
     xa = np.abs(_dequant_x(xq[rows], xds[rows]))
-    sa = np.abs(xds[rows][..., 1].view(np.float16).astype(np.float64))
+    sa = np.abs(_msums(cfg.wtype, xds[rows]))
     for i, r in enumerate(rows):
         e = int(row_exp[i])
         rec = wl.arena[e * st:e * st + wl.rec_bytes]
@@ -180,13 +213,17 @@ def mmq_error_bound(cfg, stage: str) -> float:
     """Relative bound (times abs_dot_bound) on |GPU - oracle| for one output of a
     grouped MMQ stage, whatever the tensor-core kernel.  The folded-scale kernel
     accumulates every product in TMEM: 3 MMAs per 16-wide K step (2 for Q2_0,
-    whose weights are exact in one binary16) plus one per 16 blocks for the Q4_1
-    m term, each fp32 accumulation off by at most one ulp of the running sum
-    (which abs_dot_bound bounds), and it drops the lo*lo product (below 2^-22 of
-    each term).  The oracle rounds once per block (half an ulp)."""
+    whose weights are exact in one binary16) plus one per 16 m-term entries (one
+    per block for Q4_1, per 16 values for Q2_K), each fp32 accumulation off by at
+    most one ulp of the running sum (which abs_dot_bound bounds), and it drops
+    the lo*lo product (below 2^-22 of each term).  The oracle rounds once per
+    block step (half an ulp): one step per block, two for Q4_1, three for Q2_K."""
     k = cfg.d if stage == "gateup" else cfg.f
     nb = k // 32
     n_acc = (2 if cfg.wtype == mw.Q2_0 else 3) * (k // 16)
     if cfg.wtype == mw.Q4_1:
         n_acc += (nb + 15) // 16
-    return (n_acc + nb) * 2.0 ** -23 + 2.0 ** -22
+    if cfg.wtype == mw.Q2_K:
+        n_acc += (k // 16 + 15) // 16
+    n_oracle = nb * {mw.Q4_1: 2, mw.Q2_K: 3}.get(cfg.wtype, 1)
+    return (n_acc + n_oracle) * 2.0 ** -23 + 2.0 ** -22

@@ -116,9 +116,9 @@ def test_canary_tiny_all_paths():
     _case(mw.Q8_0, 7, 2, 16, 256, 128, 41)
 
 
-@pytest.mark.parametrize("wtype", [mw.Q4_1, mw.Q2_0])
+@pytest.mark.parametrize("wtype", [mw.Q4_1, mw.Q2_0, mw.Q2_K])
 def test_canary_other_formats(wtype):
-    _case(wtype, 300, 4, 40, 256, 128, 42)
+    _case(wtype, 300, 4, 40, 256, 256 if wtype == mw.Q2_K else 128, 42)
 
 
 def test_canary_ragged_and_dropped():

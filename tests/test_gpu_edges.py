@@ -56,9 +56,9 @@ def test_no_routed_expert(streamed):
     assert bits & m.DEV_ERR_BAD_EXPERT_ID
 
 
-@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0])
+@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0, mw.Q2_K])
 def test_single_token_single_expert(wtype):
-    E, d, f = 4, 256, 128
+    E, d, f = 4, 256, 256 if wtype == mw.Q2_K else 128
     arena, rb, stride, x, _, _ = _problem(wtype, 1, d, f, E, 1, 22)
     ids = np.array([[3]], np.int32)
     w = np.array([[1.0]], np.float32)
@@ -82,6 +82,27 @@ def test_ragged_expert_sizes(streamed):
     assert bits == 0
     ref = _oracle(mw.Q8_0, E, d, f, arena, rb, stride, x, ids, w)
     assert H.rel_l2_rows(out, ref).max() <= 2e-3
+
+
+@pytest.mark.parametrize("path", [None, "simt"])
+def test_ragged_expert_sizes_q2_k(path, monkeypatch):
+    """Q2_K (D2S6 activations) on experts with 1 .. 257 rows, K = 2, three
+    super-blocks of d and two of f, on the tensor cores and on the CUDA cores."""
+    if path:
+        monkeypatch.setenv("MOE_MMQ_PATH", path)
+    sizes = [1, 15, 16, 17, 127, 128, 129, 257]
+    E, d, f = len(sizes) + 2, 768, 512
+    ids = np.concatenate([np.full(n, e + 1, np.int32) for e, n in enumerate(sizes)])
+    ids = np.random.default_rng(4).permutation(ids)
+    ids = ids[: ids.size // 2 * 2].reshape(-1, 2)
+    T = ids.shape[0]
+    arena, rb, stride, x, _, w = _problem(mw.Q2_K, T, d, f, E, 2, 25, ids=ids)
+    x[5] = 0.0
+    out, bits = _run(mw.Q2_K, E, d, f, arena, rb, stride, x, ids, w)
+    assert bits == 0
+    ref = _oracle(mw.Q2_K, E, d, f, arena, rb, stride, x, ids, w)
+    assert H.rel_l2_rows(out, ref).max() <= 2e-3
+    assert not out[5].any()
 
 
 @pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0])

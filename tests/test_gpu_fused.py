@@ -61,7 +61,7 @@ def _assert_same(a, b):
 
 
 @pytest.mark.parametrize("name", [mw.TINY.name, mw.T600.name, mw.T2048.name, mw.T2048_Q2.name,
-                                  mw.T8192.name])
+                                  mw.T2048_Q2K.name, mw.T8192.name])
 def test_fused_equals_seven_calls(name):
     wl = H.workload(name)
     cfg = wl.cfg
@@ -168,7 +168,8 @@ def test_fused_layer_matches_oracle(name):
         assert not out[t].any()
 
 
-@pytest.mark.parametrize("name", [mw.TINY.name, mw.T600.name, mw.T2048.name, mw.T2048_Q2.name])
+@pytest.mark.parametrize("name", [mw.TINY.name, mw.T600.name, mw.T2048.name, mw.T2048_Q2.name,
+                                  mw.T2048_Q2K.name])
 def test_down_combine_matches_oracle(name):
     """moe_grouped_mmq_down_combine alone, on hidden rows quantized by the
     oracle: its combined output against the oracle's down product followed by
@@ -182,7 +183,7 @@ def test_down_combine_matches_oracle(name):
     assert R == T * K
     hid = mw.normal_f32(cfg.seed, 9, R * f, scale=0.05).reshape(R, f)
     hid[::53] = 0.0
-    hq, hds = oracle.requant_hidden_q8_1(hid)
+    hq, hds = oracle.requant_hidden_q8_1(hid, layout=oracle.layout_of(cfg.wtype))
     layer = m.MoeLayer(cfg.wtype, cfg.E, d, f, K, T, H.to_dev(wl.arena), wl.rec_bytes,
                        wl.arena_stride)
     layer.forward(H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w))  # slot map, group buffers

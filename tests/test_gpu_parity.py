@@ -95,22 +95,24 @@ def test_slot_map_empty():
 
 # ----------------------------------------------------------------- stage 2 --
 
-def _quant_gpu(x, slot, K, R):
+def _quant_gpu(x, slot, K, R, wtype=m.MOE_W_Q8_0):
     T, d = x.shape
     q = torch.full((max(R, 1), d), 0x55, dtype=torch.int8, device="cuda")
-    ds = torch.full((max(R, 1), d // 32, 2), 0x55, dtype=torch.int16, device="cuda")
-    m.moe_quantize_scatter_q8_1(H.to_dev(x), H.to_dev(slot), K, R, q, ds)
+    ds = torch.full((max(R, 1), d // 32, m.ds_halves(wtype)), 0x55, dtype=torch.int16, device="cuda")
+    m.quantizers(wtype)[0](H.to_dev(x), H.to_dev(slot), K, R, q, ds)
     return q.cpu().numpy()[:R], H.u16(ds)[:R]
 
 
 @pytest.mark.parametrize("name", ALL)
 def test_quantize_scatter(name):
+    """Stage 2 in the layout the workload's weight type reads (D2S6 for Q2_K)."""
     wl = H.workload(name)
     cfg = wl.cfg
     o = oracle.build_slot_map(wl.ids, cfg.E)
     R = int(o["offsets"][cfg.E])
-    q, ds = _quant_gpu(wl.x, o["slot"], cfg.K, R)
-    qo, dso = oracle.quantize_scatter_q8_1(wl.x, o["slot"], cfg.K, R)
+    q, ds = _quant_gpu(wl.x, o["slot"], cfg.K, R, cfg.wtype)
+    qo, dso = oracle.quantize_scatter_q8_1(wl.x, o["slot"], cfg.K, R,
+                                           layout=oracle.layout_of(cfg.wtype))
     assert np.array_equal(q, qo)
     assert np.array_equal(ds, dso)
     for t in cfg.zero_list():
@@ -118,22 +120,24 @@ def test_quantize_scatter(name):
         assert not q[rows].any() and not ds[rows].any()
 
 
+@pytest.mark.parametrize("wtype", [m.MOE_W_Q8_0, m.MOE_W_Q2_K])
 @pytest.mark.parametrize("T", [1, 2, 7, 600, 2099])
-def test_scatter_equals_gather_on_gpu(T):
+def test_scatter_equals_gather_on_gpu(T, wtype):
     """Identity of the scatter and the per-row gather quantizer, both on the GPU
-    (10 of 512 experts, one all-zero token), and against the oracle."""
+    (10 of 512 experts, one all-zero token), and against the oracle, in the
+    (d, s) layout and in D2S6 (the layout Q2_K weights read)."""
     d, K, E = 2048, 10, 512
     x = mw.normal_f32(0x77 + T, 1, T * d).reshape(T, d)
     x[T // 3] = 0.0
     ids, _ = mw.topk_softmax(mw.normal_f32(0x77 + T, 2, T * E).reshape(T, E), K)
     o = oracle.build_slot_map(ids, E)
     R = T * K
-    qs, dss = _quant_gpu(x, o["slot"], K, R)
+    qs, dss = _quant_gpu(x, o["slot"], K, R, wtype)
     q = torch.zeros((R, d), dtype=torch.int8, device="cuda")
-    ds = torch.zeros((R, d // 32, 2), dtype=torch.int16, device="cuda")
-    m.moe_quantize_gather_q8_1(H.to_dev(x), H.to_dev(o["src"]), R, q, ds)
+    ds = torch.zeros((R, d // 32, m.ds_halves(wtype)), dtype=torch.int16, device="cuda")
+    m.quantizers(wtype)[1](H.to_dev(x), H.to_dev(o["src"]), R, q, ds)
     assert np.array_equal(qs, q.cpu().numpy()) and np.array_equal(dss, H.u16(ds))
-    qo, dso = oracle.quantize_gather_q8_1(x, o["src"])
+    qo, dso = oracle.quantize_gather_q8_1(x, o["src"], layout=oracle.layout_of(wtype))
     assert np.array_equal(qs, qo) and np.array_equal(dss, dso)
 
 
@@ -148,6 +152,31 @@ def test_quantizer_golden_blocks_on_gpu():
     for i, c in enumerate(cases):
         assert np.array_equal(q[i, :32], c["q"]), c["name"]
         assert ds[i, 0, 0] == c["d"] and ds[i, 0, 1] == c["s"], c["name"]
+
+
+def test_quantizer_d2s6_golden_blocks_on_gpu():
+    """The hand-derived D2S6 blocks through the scatter, the gather and the
+    hidden-row quantizer."""
+    from tests.test_oracle_pins import _golden_blocks
+    cases = _golden_blocks("q8_1_d2s6_blocks.txt")
+    x = np.stack([c["x"] for c in cases]).reshape(len(cases), 32)
+    x = np.concatenate([np.zeros((len(cases), 32), np.float32), x], 1)  # block 1 of width 64
+    R = len(cases)
+    idx = np.arange(R, dtype=np.int32)
+    res = [_quant_gpu(x, idx, 1, R, m.MOE_W_Q2_K)]
+    for which in (1, 2):
+        q = torch.zeros((R, 64), dtype=torch.int8, device="cuda")
+        ds = torch.zeros((R, 2, 4), dtype=torch.int16, device="cuda")
+        if which == 1:
+            m.moe_quantize_gather_q8_1_d2s6(H.to_dev(x), H.to_dev(idx), R, q, ds)
+        else:
+            m.moe_requant_hidden_q8_1_d2s6(H.to_dev(x), R, 64, q, ds)
+        res.append((q.cpu().numpy(), H.u16(ds)))
+    for q, ds in res:
+        for i, c in enumerate(cases):
+            assert np.array_equal(q[i, 32:], c["q"]), c["name"]
+            assert list(ds[i, 1]) == [c["d"], c["s"], c["slo"], c["shi"]], c["name"]
+            assert not q[i, :32].any() and not ds[i, 0].any()
 
 
 def test_quantize_skips_rows_out_of_range():
@@ -236,7 +265,8 @@ def test_mmq_gateup(name):
     cfg = wl.cfg
     o = oracle.build_slot_map(wl.ids, cfg.E)
     R = int(o["offsets"][cfg.E])
-    q, ds = oracle.quantize_scatter_q8_1(wl.x, o["slot"], cfg.K, R)
+    q, ds = oracle.quantize_scatter_q8_1(wl.x, o["slot"], cfg.K, R,
+                                         layout=oracle.layout_of(cfg.wtype))
     h = _mmq_gpu("gateup", wl, o, q, ds)
     assert np.isfinite(h).all()
     rows = np.arange(R) if R <= 64 else H.sample_rows(o["offsets"], o["active"], o["n_active"], 96, 1)
@@ -256,7 +286,7 @@ def test_mmq_down(name):
     # hidden rows from the generator (scaled like SiLU(g)*u), quantized by the oracle
     hid = mw.normal_f32(cfg.seed, 9, R * cfg.f, scale=0.05).reshape(R, cfg.f)
     hid[::53] = 0.0
-    hq, hds = oracle.requant_hidden_q8_1(hid)
+    hq, hds = oracle.requant_hidden_q8_1(hid, layout=oracle.layout_of(cfg.wtype))
     y = _mmq_gpu("down", wl, o, hq, hds)
     rows = np.arange(R) if R <= 64 else H.sample_rows(o["offsets"], o["active"], o["n_active"], 96, 2)
     ref = H.oracle_rows("down", wl, o["offsets"], hq, hds, rows)
@@ -269,7 +299,7 @@ def test_mmq_down(name):
 
 @pytest.mark.parametrize("stage", ["gateup", "down"])
 @pytest.mark.parametrize("name", [mw.TINY.name, mw.T600.name, mw.T2048.name, mw.T8192.name,
-                                  mw.T2048_Q2.name])
+                                  mw.T2048_Q2.name, mw.T2048_Q2K.name])
 def test_mmq_tensor_cores_match_cuda_cores(name, stage, monkeypatch):
     """The per-block-scaling tcgen05 kernel forms each block's integer dot exactly
     and scales it in the same fp32 order as the dp4a kernel, so the two agree bit
@@ -280,11 +310,12 @@ def test_mmq_tensor_cores_match_cuda_cores(name, stage, monkeypatch):
     cfg = wl.cfg
     o = oracle.build_slot_map(wl.ids, cfg.E)
     R = int(o["offsets"][cfg.E])
+    lay = oracle.layout_of(cfg.wtype)
     if stage == "gateup":
-        xq, xds = oracle.quantize_scatter_q8_1(wl.x, o["slot"], cfg.K, R)
+        xq, xds = oracle.quantize_scatter_q8_1(wl.x, o["slot"], cfg.K, R, layout=lay)
     else:
         hid = mw.normal_f32(cfg.seed, 9, R * cfg.f, scale=0.05).reshape(R, cfg.f)
-        xq, xds = oracle.requant_hidden_q8_1(hid)
+        xq, xds = oracle.requant_hidden_q8_1(hid, layout=lay)
     monkeypatch.setenv("MOE_MMQ_PATH", "blockscale")
     bs = _mmq_gpu(stage, wl, o, xq, xds)
     monkeypatch.setenv("MOE_MMQ_PATH", "simt")
@@ -310,9 +341,9 @@ def test_requant_hidden(name):
     hid[::31] = 0.0
     hid[5, :32] = np.float32(2.0 ** -130)
     hq = torch.zeros((R, cfg.f), dtype=torch.int8, device="cuda")
-    hds = torch.zeros((R, cfg.f // 32, 2), dtype=torch.int16, device="cuda")
-    m.moe_requant_hidden_q8_1(H.to_dev(hid), R, cfg.f, hq, hds)
-    ro, rdo = oracle.requant_hidden_q8_1(hid)
+    hds = torch.zeros((R, cfg.f // 32, m.ds_halves(cfg.wtype)), dtype=torch.int16, device="cuda")
+    m.quantizers(cfg.wtype)[2](H.to_dev(hid), R, cfg.f, hq, hds)
+    ro, rdo = oracle.requant_hidden_q8_1(hid, layout=oracle.layout_of(cfg.wtype))
     assert np.array_equal(hq.cpu().numpy(), ro) and np.array_equal(H.u16(hds), rdo)
 
 

@@ -28,7 +28,8 @@ def _layer(wl):
 
 
 @pytest.mark.parametrize("name,ring_groups", [(mw.TINY.name, 1), (mw.T600.name, 1),
-                                              (mw.T600.name, 3), (mw.T2048.name, 2)])
+                                              (mw.T600.name, 3), (mw.T2048.name, 2),
+                                              (mw.T2048_Q2K.name, 2)])
 def test_streamed_equals_resident(name, ring_groups):
     wl = H.workload(name)
     layer = _layer(wl)

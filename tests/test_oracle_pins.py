@@ -9,7 +9,8 @@ Pages cited (pull requests of the "Strata" engine):
   #1368 "quantize each token's MoE input once and scatter it to its k rows",
         intro (slot[t*K+k], the inverse of src) and "Identity" (scatter equals
         the per-row gather quantization byte for byte at T = 1, 2, 7, 600, 2099,
-        10 of 512 experts, one all-zero token).
+        10 of 512 experts, one all-zero token; D2S6 is the layout that
+        serves Q2_K, and the Q2_0 / Q2_K names).
   #439  "a group's expert gathers in one launch", "What" (the batch equals one
         copy per expert byte for byte: 1-16 experts, mid-group starts,
         unaligned / odd sizes).
@@ -67,9 +68,9 @@ def test_f16_rounding_against_numpy():
 
 # ---------------------------------------------------------------- quantizer --
 
-def _golden_blocks():
+def _golden_blocks(name="q8_1_blocks.txt"):
     cases, cur = [], None
-    with open(os.path.join(GOLDEN, "q8_1_blocks.txt")) as fh:
+    with open(os.path.join(GOLDEN, name)) as fh:
         for line in fh:
             line = line.strip()
             if not line or line.startswith("#"):
@@ -134,6 +135,58 @@ def test_quantizer_invariants_random():
         assert np.all(np.abs(r - q) <= 0.5 + 1e-6)
         assert dh == int(_np_f16_bits(d32))
         assert sh == int(_np_f16_bits(d32 * np.float32(q.astype(np.int64).sum())))
+
+
+@pytest.mark.parametrize("case", _golden_blocks("q8_1_d2s6_blocks.txt"), ids=lambda c: c["name"])
+def test_quantizer_d2s6_golden_blocks(case):
+    q, e = oracle.quantize_block_q8_1_d2s6(case["x"])
+    assert np.array_equal(q, case["q"])
+    assert [int(v) for v in e] == [case["d"], case["s"], case["slo"], case["shi"]]
+
+
+def test_quantizer_d2s6_invariants_random():
+    """D2S6 carries the q8_1 block unchanged (quants, d, s equal the (d, s)
+    quantizer's) plus the half sums; a block whose second (first) half is zero
+    has s_lo == s and s_hi == 0 (s_lo == 0, s_hi == s); a block whose halves are
+    negatives of each other has s == 0 and s_lo == -s_hi; and s_lo + s_hi stays
+    within the binary16 rounding of s."""
+    rng = np.random.default_rng(12)
+    x = (rng.normal(size=(3000, 32)) * rng.lognormal(0, 2, size=(3000, 1))).astype(np.float32)
+    x[0:500, 16:] = 0.0
+    x[500:1000, :16] = 0.0
+    x[1000:1500, 16:] = -x[1000:1500, :16]
+    for i, v in enumerate(x):
+        q, e = oracle.quantize_block_q8_1_d2s6(v)
+        q1, dh, sh = oracle.quantize_block_q8_1(v)
+        assert np.array_equal(q, q1) and int(e[0]) == dh and int(e[1]) == sh
+        f = e.view(np.float16).astype(np.float64)
+        if i < 500:
+            assert e[2] == e[1] and f[3] == 0.0
+        elif i < 1000:
+            assert e[3] == e[1] and f[2] == 0.0
+        elif i < 1500:
+            assert f[1] == 0.0 and f[2] == -f[3]
+        assert abs(f[2] + f[3] - f[1]) <= 2 * 2.0 ** -11 * (abs(f[2]) + abs(f[3]) + abs(f[1]))
+
+
+def test_scatter_equals_gather_identity_d2s6():
+    """#1368 Identity for the D2S6 layout: scatter == per-row gather on the
+    whole buffer; requant of the gathered token rows gives the same bytes."""
+    T, d, K, E = 300, 256, 10, 512
+    x = mw.normal_f32(0xD256, 1, T * d).reshape(T, d)
+    x[7] = 0.0
+    ids, _ = mw.topk_softmax(mw.normal_f32(0xD256, 2, T * E).reshape(T, E), K)
+    sm = oracle.build_slot_map(ids, E)
+    R = int(sm["offsets"][E])
+    L = oracle.LAYOUT_D2S6
+    qs, dss = oracle.quantize_scatter_q8_1(x, sm["slot"], K, R, fill=0x55, layout=L)
+    qg, dsg = oracle.quantize_gather_q8_1(x, sm["src"], layout=L)
+    qh, dsh = oracle.requant_hidden_q8_1(x[sm["src"]], layout=L)
+    assert dss.shape == (R, d // 32, 4)
+    assert np.array_equal(qs, qg) and np.array_equal(dss, dsg)
+    assert np.array_equal(qs, qh) and np.array_equal(dss, dsh)
+    q2, ds2 = oracle.quantize_gather_q8_1(x, sm["src"])
+    assert np.array_equal(qs, q2) and np.array_equal(dss[..., :2], ds2)
 
 
 # ------------------------------------------------------------------ slot map --
@@ -259,9 +312,11 @@ def _silu_mul64(g, u):
         return g / (1.0 + np.exp(-g)) * u
 
 
-@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0])
+@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0, mw.Q2_K])
 def test_record_layout_agrees(wtype):
-    for d, f in ((256, 128), (2048, 768), (96, 64)):
+    sizes = ((256, 256), (2048, 768), (512, 1280)) if wtype == mw.Q2_K else \
+        ((256, 128), (2048, 768), (96, 64))
+    for d, f in sizes:
         assert oracle.expert_record_bytes(wtype, d, f) == mw.record_bytes(wtype, d, f)
         assert oracle.record_offsets(wtype, d, f) == _mat_offsets(wtype, d, f)
     # sizes worked out by hand: 3*f*d*34/32 and 3*f*d*20/32 at d=2048, f=768
@@ -269,6 +324,8 @@ def test_record_layout_agrees(wtype):
     assert oracle.expert_record_bytes(mw.Q4_1, 2048, 768) == 2949120
     # Q2_0: 3*f*d*(2/8 + 2/32)
     assert oracle.expert_record_bytes(mw.Q2_0, 2048, 768) == 1474560
+    # Q2_K: 3*f*d*(2/8 + 2*2/256 + 1/16)
+    assert oracle.expert_record_bytes(mw.Q2_K, 2048, 768) == 1548288
 
 
 def _small_problem(wtype, T=9, d=128, f=96, E=5, K=2, seed=11):
@@ -279,20 +336,22 @@ def _small_problem(wtype, T=9, d=128, f=96, E=5, K=2, seed=11):
     return arena, rb, stride, x, ids, w
 
 
-@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0])
+@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0, mw.Q2_K])
 def test_mmq_against_dequantized_matmul(wtype):
     """The block-scaled integer dot equals the product of the dequantized
-    matrices (w = d*q (+m), x = d_x*q_x), computed by a plain fp64 matmul.  For
-    Q4_1 the method uses s = fp16(d_x * sum q_x) in the m term, so the two differ
-    by at most |m| * |s - fp16(d_x) * sum q_x| per block."""
-    d, f, E = 128, 96, 5
+    matrices (w = d*q (+m), Q2_K w = d*sc*c - dmin*mn; x = d_x*q_x), computed by
+    a plain fp64 matmul.  For Q4_1 (Q2_K) the method uses s = fp16(d_x * sum q_x)
+    over each 32-block (16-value half) in the m term, so the two differ by at most
+    |m| * |s - fp16(d_x) * sum q_x| per block (half)."""
+    d, f, E = (512, 256, 5) if wtype == mw.Q2_K else (128, 96, 5)
     arena, rb, stride, x, ids, w = _small_problem(wtype, d=d, f=f, E=E)
     sm = oracle.build_slot_map(ids, E)
     R = int(sm["offsets"][E])
-    q, ds = oracle.quantize_scatter_q8_1(x, sm["slot"], ids.shape[1], R)
+    lay = oracle.layout_of(wtype)
+    q, ds = oracle.quantize_scatter_q8_1(x, sm["slot"], ids.shape[1], R, layout=lay)
     gb = oracle.gather_groups(arena, rb, stride, sm["active"], sm["n_active"], rb)
     h = oracle.grouped_mmq_gateup(wtype, gb, rb, sm["active"], sm["n_active"], sm["offsets"], q, ds, d, f)
-    hq, hds = oracle.requant_hidden_q8_1(h)
+    hq, hds = oracle.requant_hidden_q8_1(h, layout=lay)
     y = oracle.grouped_mmq_down(wtype, gb, rb, sm["active"], sm["n_active"], sm["offsets"], hq, hds, d, f)
     og, ou, od = _mat_offsets(wtype, d, f)
     xq = _dequant_x(q, ds)
@@ -311,11 +370,17 @@ def test_mmq_against_dequantized_matmul(wtype):
         tol_g = 1e-5 * (np.abs(xq[rows]) @ np.abs(_dequant_w(Gq, Gd, Gm)).T) + 1e-30
         tol_u = 1e-5 * (np.abs(xq[rows]) @ np.abs(_dequant_w(Uq, Ud, Um)).T) + 1e-30
         tol_y = 1e-5 * (np.abs(hx[rows]) @ np.abs(_dequant_w(Dq, Dd, Dm)).T) + 1e-30
-        if wtype == mw.Q4_1:
+        if wtype in (mw.Q4_1, mw.Q2_K):
             def sbound(qx, dsx, m):
                 dx = dsx[..., 0].view(np.float16).astype(np.float64)
-                sx = dsx[..., 1].view(np.float16).astype(np.float64)
-                err = np.abs(sx - dx * qx.reshape(qx.shape[0], -1, 32).sum(-1))
+                if wtype == mw.Q2_K:  # (s_lo, s_hi) against each 16-value half
+                    sx = dsx[..., 2:4].view(np.float16).astype(np.float64).reshape(qx.shape[0], -1)
+                    dx = np.repeat(dx, 2, axis=1)
+                    width = 16
+                else:
+                    sx = dsx[..., 1].view(np.float16).astype(np.float64)
+                    width = 32
+                err = np.abs(sx - dx * qx.reshape(qx.shape[0], -1, width).sum(-1))
                 return err @ np.abs(m).T
             tol_g += sbound(q[rows], ds[rows], Gm)
             tol_u += sbound(q[rows], ds[rows], Um)
@@ -454,16 +519,71 @@ def test_mmq_q2_0_integer_special_case():
     assert np.array_equal(y.astype(np.float64), ref.astype(np.float64))
 
 
+def test_mmq_q2_k_integer_special_case():
+    """Q2_K with power-of-two scales, packed here by hand: codes as for Q2_0,
+    super-block d and dmin planes [k/256][rows], sub-block bytes sc | mn << 4
+    [k/16][rows]; activations with d_x = 1 and exact half sums.  Every term is
+    then a multiple of 1/2 below 2^23, so the down product equals the exact
+    matrix product with the weights d*sc*c - dmin*mn.  Distinct d and dmin per
+    super-block and random sc, mn per sub-block pin the plane order, the
+    nibbles, the super-block index and the sign and halves of the min term."""
+    d, f, E = 64, 512, 2
+    rng = np.random.default_rng(17)
+    rb = oracle.expert_record_bytes(mw.Q2_K, d, f)
+    og, ou, od = _mat_offsets(mw.Q2_K, d, f)
+    a128 = lambda v: (v + 127) // 128 * 128
+    recs = np.zeros(E * rb, np.uint8)
+    Wd = []
+    for e in range(E):
+        c = rng.integers(0, 4, (d, f))
+        sc = rng.integers(0, 16, (d, f // 16))
+        mn = rng.integers(0, 16, (d, f // 16))
+        dd = rng.choice([1.0, 2.0], (d, f // 256))
+        dm = rng.choice([0.5, 4.0], (d, f // 256))
+        Wd.append(np.repeat(dd, 256, axis=1) * np.repeat(sc, 16, axis=1) * c
+                  - np.repeat(dm, 256, axis=1) * np.repeat(mn, 16, axis=1))
+        packed = np.zeros((d, f // 4), np.uint8)
+        for j in range(f // 4):
+            for i in range(4):
+                packed[:, j] |= (c[:, 4 * j + i] << (2 * i)).astype(np.uint8)
+        base = e * rb + od
+        recs[base:base + d * f // 4] = packed.ravel()
+        o = base + a128(d * f // 4)
+        sb = d * (f // 256) * 2
+        recs[o:o + sb] = dd.T.astype(np.float16).ravel().view(np.uint8)
+        o += a128(sb)
+        recs[o:o + sb] = dm.T.astype(np.float16).ravel().view(np.uint8)
+        o += a128(sb)
+        recs[o:o + d * (f // 16)] = (sc | (mn << 4)).T.astype(np.uint8).ravel()
+    R = 9
+    hq = rng.integers(-127, 128, (R, f)).astype(np.int8)
+    halves = hq.astype(np.int64).reshape(R, f // 32, 2, 16).sum(-1)
+    hds = np.zeros((R, f // 32, 4), np.uint16)
+    hds[..., 0] = 0x3C00
+    hds[..., 1] = halves.sum(-1).astype(np.float16).view(np.uint16)
+    hds[..., 2:4] = halves.astype(np.float16).view(np.uint16)  # |half| <= 2032: exact
+    offsets = np.array([0, 4, 9], np.int32)
+    active = np.array([0, 1], np.int32)
+    y = oracle.grouped_mmq_down(mw.Q2_K, recs, rb, active, 2, offsets, hq, hds, d, f)
+    ref = np.concatenate([hq[0:4].astype(np.float64) @ Wd[0].T, hq[4:9].astype(np.float64) @ Wd[1].T])
+    assert np.array_equal(y.astype(np.float64), ref)
+    # the numpy decoder of the tests reads the same record the same way
+    q, dpl, mpl = _planes(mw.Q2_K, recs[:rb], od, d, f)
+    assert np.array_equal(_dequant_w(q, dpl, mpl), Wd[0])
+
+
 # ------------------------------------------------------------ end to end ---
 
-@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0])
+@pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0, mw.Q2_K])
 def test_layer_end_to_end_tiny(wtype):
     """Tiny layer: the all-zero token gives an exactly zero row, and the whole
     layer agrees with an unquantized fp64 pipeline (dequantized weights, raw
     activations and hidden rows) to within the 8-bit quantization noise."""
     cfg = mw.TINY
-    wl = mw.make_workload(mw.Config(cfg.name, cfg.T, cfg.d, cfg.f, cfg.E, cfg.K, wtype, cfg.seed,
-                                    zero_tokens=cfg.zero_tokens))
+    f = 256 if wtype == mw.Q2_K else cfg.f  # Q2_K super-blocks need k % 256 == 0
+    cfg = mw.Config(cfg.name, cfg.T, cfg.d, f, cfg.E, cfg.K, wtype, cfg.seed,
+                    zero_tokens=cfg.zero_tokens)
+    wl = mw.make_workload(cfg)
     r = oracle.layer_forward(wtype, wl.arena, wl.rec_bytes, wl.arena_stride, wl.x, wl.ids, wl.w,
                              cfg.E, cfg.d, cfg.f)
     assert not r["out"][3].any()
