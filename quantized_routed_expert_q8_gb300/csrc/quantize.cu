@@ -54,7 +54,12 @@ __device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
     // d == 0 (amax == 0, or an fp32-subnormal amax <= 63 * 2^-149 whose quotient
     // underflows) leaves x / d undefined: such a block is stored as all-zero
     const float d = __fdiv_rn(amax, 127.0f);
-    if (d != 0.0f) {
+    // d differs between the blocks of a warp (and is zero in some), so every
+    // warp-collective operation below sits outside the branches on d
+    const bool nz = d != 0.0f;
+    float x[16];
+    uint32_t need = 0u;  // values whose quotient must be formed exactly
+    if (nz) {
         // q = round-half-away(fp32(v / d)).  With a normal d, qa = v * RN(1/d) is
         // within 3 ulp of the IEEE quotient, and |qa| < 128 puts an ulp at
         // <= 2^-17; so unless qa lies within 2^-14 of a half-integer, rounding qa
@@ -62,8 +67,7 @@ __device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
         // a subnormal d) the quotient itself is formed with an IEEE division.
         const bool fast_ok = d >= 1.17549435e-38f;
         const float r = fast_ok ? __frcp_rn(d) : 0.0f;
-        float x[16];
-        uint32_t need = fast_ok ? 0u : 0xFFFFu;  // values whose quotient must be exact
+        if (!fast_ok) need = 0xFFFFu;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const float qa = __fmul_rn(v[i], r);
@@ -71,13 +75,15 @@ __device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
             x[i] = roundf(qa);
             if (fabsf(fr - 0.5f) <= 6.103515625e-05f) need |= 1u << i;
         }
-        // a warp-uniform branch, so that the divisions run only in the rare
-        // warps that need one
-        if (__any_sync(0xffffffffu, need != 0u)) {
+    }
+    // a warp-uniform branch (every lane votes), so that the divisions run only
+    // in the rare warps that need one; need is zero where d is
+    if (__any_sync(0xffffffffu, need != 0u)) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if ((need >> i) & 1u) x[i] = roundf(__fdiv_rn(v[i], d));
-        }
+        for (int i = 0; i < 16; ++i)
+            if ((need >> i) & 1u) x[i] = roundf(__fdiv_rn(v[i], d));
+    }
+    if (nz) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int qi = (int)fminf(127.0f, fmaxf(-127.0f, x[i]));
