@@ -169,8 +169,9 @@ def pci_bus_id(dev):
 # ------------------------------------------------------------ bytes / ops --
 
 # FP32 operations per block-scale partial in the MMQ epilogue: fma(dW*dX, I, acc)
-# is a multiply and an FMA; Q4_1 adds fma(mW, sX, acc).
-ALU_OPS_PER_PARTIAL = {0: 2, 1: 3, 2: 2}  # by weight type (Q8_0, Q4_1, Q2_0)
+# is a multiply and an FMA; Q4_1 adds fma(mW, sX, acc), Q2_K two such FMAs (one
+# per 16-value half).
+ALU_OPS_PER_PARTIAL = {0: 2, 1: 3, 2: 2, 3: 4}  # by weight type (Q8_0, Q4_1, Q2_0, Q2_K)
 FP32_LANES_PER_SM = 128
 MAX_SM_MHZ = 2070.0  # GB300 maximum SM clock
 

@@ -34,6 +34,13 @@ struct Q8Half {
     __half2 lh;   // D2S6 (s_lo, s_hi), valid in the first-half lane
 };
 
+// byte permute: result byte i = byte (sel >> 4i) & 7 of {a, b} (a bytes 0-3)
+__device__ __forceinline__ uint32_t prmt_bytes(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
 template <bool D2S6>
 __device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
     float v[16];
@@ -49,48 +56,59 @@ __device__ __forceinline__ Q8Half quantize16(const float4 (&a)[4]) {
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     Q8Half r;
-    int sum = 0;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
     // d == 0 (amax == 0, or an fp32-subnormal amax <= 63 * 2^-149 whose quotient
     // underflows) leaves x / d undefined: such a block is stored as all-zero
     const float d = __fdiv_rn(amax, 127.0f);
-    // d differs between the blocks of a warp (and is zero in some), so every
-    // warp-collective operation below sits outside the branches on d
     const bool nz = d != 0.0f;
-    float x[16];
-    uint32_t need = 0u;  // values whose quotient must be formed exactly
-    if (nz) {
-        // q = round-half-away(fp32(v / d)).  With a normal d, qa = v * RN(1/d) is
-        // within 3 ulp of the IEEE quotient, and |qa| < 128 puts an ulp at
-        // <= 2^-17; so unless qa lies within 2^-14 of a half-integer, rounding qa
-        // gives the same integer as rounding the quotient.  Otherwise (and for
-        // a subnormal d) the quotient itself is formed with an IEEE division.
-        const bool fast_ok = d >= 1.17549435e-38f;
-        const float r = fast_ok ? __frcp_rn(d) : 0.0f;
-        if (!fast_ok) need = 0xFFFFu;
+    // q = round-half-away(fp32(v / d)).  With a normal d, qa = RN(v * RN(1/d))
+    // is within 3 ulp of the IEEE quotient (|qa| < 127.0001, so within 2.3e-5),
+    // hence unless qa lies within 2^-14 of a half-integer, the nearest integer
+    // to qa is the rounded quotient, and no tie can occur, so round-to-nearest-
+    // even and round-half-away agree.  That integer comes from one addition of
+    // M = 1.5 * 2^23: qa + M lies in [2^23, 2^24), where the spacing is 1, so
+    // its bits are 0x4B400000 + q (q in [-127, 127]; the low byte is q's int8
+    // byte) and (qa + M) - M = q exactly.  A lane whose block has a subnormal d,
+    // or one of whose values lies within 2^-14 of a half-integer
+    // (|qa - q| >= 0.5 - 2^-14), forms the IEEE quotients instead.
+    constexpr float M = 12582912.0f;
+    constexpr uint32_t MB = 0x4B400000u;  // bits of M
+    const bool fast_ok = d >= 1.17549435e-38f;
+    const float rc = fast_ok ? __frcp_rn(d) : 0.0f;
+    uint32_t bq[16];  // bits of q + M
+    float off = 0.0f;  // max |qa - q|
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float qa = __fmul_rn(v[i], r);
-            const float fr = fabsf(qa) - truncf(fabsf(qa));
-            x[i] = roundf(qa);
-            if (fabsf(fr - 0.5f) <= 6.103515625e-05f) need |= 1u << i;
+    for (int i = 0; i < 16; ++i) {
+        const float qa = __fmul_rn(v[i], rc);
+        const float t = __fadd_rn(qa, M);
+        off = fmaxf(off, fabsf(__fsub_rn(qa, __fsub_rn(t, M))));
+        bq[i] = __float_as_uint(t);
+    }
+    const bool slow = nz && (!fast_ok || off >= 0.49993896484375f);
+    // a warp-uniform branch (every lane votes; d differs between the blocks of a
+    // warp), so that the divisions run only in the rare warps that need them
+    if (__any_sync(0xffffffffu, slow)) {
+        if (slow) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float x = fminf(127.0f, fmaxf(-127.0f, roundf(__fdiv_rn(v[i], d))));
+                bq[i] = __float_as_uint(__fadd_rn(x, M));
+            }
         }
     }
-    // a warp-uniform branch (every lane votes), so that the divisions run only
-    // in the rare warps that need one; need is zero where d is
-    if (__any_sync(0xffffffffu, need != 0u)) {
+    if (!nz) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if ((need >> i) & 1u) x[i] = roundf(__fdiv_rn(v[i], d));
+        for (int i = 0; i < 16; ++i) bq[i] = MB;  // q = 0
     }
-    if (nz) {
+    // the quants are the low bytes of bq; sum(q) = sum(bq) - 16 * MB (mod 2^32)
+    uint32_t w[4], acc = 0u;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int qi = (int)fminf(127.0f, fmaxf(-127.0f, x[i]));
-            sum += qi;
-            w[i >> 2] |= (uint32_t)(qi & 0xff) << (8 * (i & 3));
-        }
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t lo = prmt_bytes(bq[4 * k], bq[4 * k + 1], 0x0040u);
+        const uint32_t hi = prmt_bytes(bq[4 * k + 2], bq[4 * k + 3], 0x0040u);
+        w[k] = prmt_bytes(lo, hi, 0x5410u);
+        acc += bq[4 * k] + bq[4 * k + 1] + bq[4 * k + 2] + bq[4 * k + 3];
     }
+    const int sum = (int)(acc - 16u * MB);
     const int other = __shfl_xor_sync(0xffffffffu, sum, 1);
     const float s = __fmul_rn(d, (float)(sum + other));
     r.q = make_uint4(w[0], w[1], w[2], w[3]);
