@@ -243,13 +243,16 @@ def alu_partials(cfg, R: int) -> float:
 PROFILED_TRAFFIC = {
     ("mmq_gateup", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/mmq_tc.cu",
-        "code_sha256_16": "abc4fd640fc3ab6c", "bytes": 610050816 + 254977792},
+        "code_sha256_16": "31258400117109e3", "bytes": 609559808 + 254505216},
     ("mmq_down", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
-        "source": "quantized_routed_expert_q8_gb300/csrc/mmq_tc.cu",
-        "code_sha256_16": "abc4fd640fc3ab6c", "bytes": 279342336 + 665958912},
+        "source": "quantized_routed_expert_q8_gb300/csrc/mmq_fold.cu",
+        "code_sha256_16": "9f291966bc921c47", "bytes": 275967232 + 666515712},
     ("quantize_scatter", "T32768_d2048_f768_E512_K10_q4_1"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/quantize.cu",
-        "code_sha256_16": "50f7d37a16a0671c", "bytes": 269889792 + 694902272},
+        "code_sha256_16": "217e4c4ac0275670", "bytes": 270006272 + 694668800},
+    ("requant_hidden", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
+        "source": "quantized_routed_expert_q8_gb300/csrc/quantize.cu",
+        "code_sha256_16": "217e4c4ac0275670", "bytes": 251683584 + 14620672},
 }
 
 
@@ -418,11 +421,12 @@ def run_gpu(args, rank, world, local_rank):
     mean_stage = stage_ms.mean(axis=0)
     phases = {n: round(float(v), 4) for n, v in zip(stage_names, mean_stage)}
     stage_roof = {n: dict(ms=round(float(v), 4),
-                          **stage_roofline(*stages[n], float(v) / 1e3, hbm, tc, peak_src))
+                          **stage_roofline(*stages[n], float(v) / 1e3, hbm, tc, peak_src),
+                          traffic=profiled_traffic(n, cfg.name))
                   for n, v in zip(stage_names, mean_stage)}
     dom = int(np.argmax(mean_stage))
     dom_name = stage_names[dom]
-    roof = {k: v for k, v in stage_roof[dom_name].items() if k != "ms"}
+    roof = {k: v for k, v in stage_roof[dom_name].items() if k not in ("ms", "traffic")}
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     alu_peak = alu_peak_ops(sms)
     t_roof = max(total_bytes / (hbm * 1e9), ops / (tc * 1e12))
