@@ -262,8 +262,12 @@ def gather_groups(arena, rec_bytes, arena_stride, active, n_active, slot_stride)
     return buf
 
 
-def layer_forward(wtype, arena, rec_bytes, arena_stride, x, ids, w, E, d, f, slot_stride=None):
-    """All seven stages in order; returns a dict of every intermediate."""
+def layer_forward(wtype, arena, rec_bytes, arena_stride, x, ids, w, E, d, f, slot_stride=None,
+                  gather=True):
+    """All seven stages in order; returns a dict of every intermediate.  With
+    gather=False stage 3 (a byte copy of the routed records, checked on its own)
+    is skipped and the two MMQ stages read every record in place in the arena
+    (active position p = expert p): the same values without the copy."""
     x = _c(x, np.float32)
     T = x.shape[0]
     K = ids.shape[1]
@@ -271,12 +275,17 @@ def layer_forward(wtype, arena, rec_bytes, arena_stride, x, ids, w, E, d, f, slo
     R = int(sm["offsets"][E])
     lay = layout_of(wtype)
     q, ds = quantize_scatter_q8_1(x, sm["slot"], K, R, layout=lay)
-    slot_stride = slot_stride or rec_bytes
-    gb = gather_groups(arena, rec_bytes, arena_stride, sm["active"], sm["n_active"], slot_stride)
-    h = grouped_mmq_gateup(wtype, gb, slot_stride, sm["active"], sm["n_active"], sm["offsets"],
-                           q, ds, d, f)
+    if gather:
+        slot_stride = slot_stride or rec_bytes
+        gb = gather_groups(arena, rec_bytes, arena_stride, sm["active"], sm["n_active"],
+                           slot_stride)
+        active, n_active = sm["active"], sm["n_active"]
+    else:
+        gb, slot_stride = arena, arena_stride
+        active, n_active = np.arange(E, dtype=np.int32), E
+    h = grouped_mmq_gateup(wtype, gb, slot_stride, active, n_active, sm["offsets"], q, ds, d, f)
     hq, hds = requant_hidden_q8_1(h, layout=lay)
-    y = grouped_mmq_down(wtype, gb, slot_stride, sm["active"], sm["n_active"], sm["offsets"],
-                         hq, hds, d, f)
+    y = grouped_mmq_down(wtype, gb, slot_stride, active, n_active, sm["offsets"], hq, hds, d, f)
     out = combine_topk(y, sm["slot"], w, T, K, d)
-    return dict(sm, q=q, ds=ds, group_buf=gb, h=h, hq=hq, hds=hds, y=y, out=out)
+    return dict(sm, q=q, ds=ds, group_buf=gb if gather else None, h=h, hq=hq, hds=hds, y=y,
+                out=out)

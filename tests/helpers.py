@@ -1,9 +1,12 @@
 """Shared helpers of the GPU parity tests: cached seeded workloads, uploads, and
 oracle sub-problems that let the CPU oracle check sampled rows and tokens of the
-full-size workloads (each token's output depends only on its own K rows)."""
+full-size workloads (each token's output depends only on its own K rows), or
+every row and token, split over one host thread per core."""
 from __future__ import annotations
 
+import concurrent.futures
 import functools
+import os
 
 import numpy as np
 
@@ -60,6 +63,56 @@ def oracle_rows(stage: str, wl: mw.Workload, offsets, xq, xds, rows):
     out = np.empty_like(res)
     out[order] = res
     return out
+
+
+def oracle_threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def _pmap(fn, parts):
+    """fn over the parts on one host thread each (the oracle's C calls release
+    the interpreter lock), results in order."""
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(parts), oracle_threads())) as ex:
+        return list(ex.map(fn, parts))
+
+
+def oracle_stage_all(stage: str, wl: mw.Workload, offsets, xq, xds) -> np.ndarray:
+    """Oracle stage 'gateup' or 'down' on every row: contiguous row ranges, one
+    per host thread, each with its own rebased offsets; the MMQ reads every
+    expert's record in place in the arena (active position p = expert p; the
+    group gather is a byte copy, checked on its own)."""
+    cfg = wl.cfg
+    E = cfg.E
+    offsets = np.asarray(offsets, np.int64)
+    R = int(offsets[E])
+    active = np.arange(E, dtype=np.int32)
+    fn = oracle.grouped_mmq_gateup if stage == "gateup" else oracle.grouped_mmq_down
+    bounds = np.linspace(0, R, min(R, 4 * oracle_threads()) + 1).astype(np.int64) if R else [0, 0]
+
+    def run(k):
+        r0, r1 = int(bounds[k]), int(bounds[k + 1])
+        off = (np.clip(offsets, r0, r1) - r0).astype(np.int32)
+        return fn(cfg.wtype, wl.arena, wl.arena_stride, active, E, off, xq[r0:r1], xds[r0:r1],
+                  cfg.d, cfg.f)
+
+    n = (cfg.f if stage == "gateup" else cfg.d)
+    if R == 0:
+        return np.zeros((0, n), np.float32)
+    return np.concatenate(_pmap(run, range(len(bounds) - 1)))
+
+
+def oracle_layer_all(wl: mw.Workload) -> np.ndarray:
+    """The oracle's layer output for every token: contiguous token slices, one
+    per host thread (tokens are independent)."""
+    cfg = wl.cfg
+    parts = [p for p in np.array_split(np.arange(wl.T), min(wl.T, 4 * oracle_threads())) if len(p)]
+
+    def run(p):
+        sub = wl.subset(p)
+        return oracle.layer_forward(cfg.wtype, wl.arena, wl.rec_bytes, wl.arena_stride, sub.x,
+                                    sub.ids, sub.w, cfg.E, cfg.d, cfg.f, gather=False)["out"]
+
+    return np.concatenate(_pmap(run, parts))
 
 
 def rel_l2_rows(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
