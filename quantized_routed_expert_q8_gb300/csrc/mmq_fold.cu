@@ -23,19 +23,22 @@
 // few units in the last place of fp32.  |d*q| must stay below 65520 (the
 // binary16 range): a block beyond it sets MOE_DEV_ERR_RANGE.
 //
-// One persistent CTA of 18 warps per SM.  A work item is up to 128 tokens of
+// One persistent CTA of 23 warps per SM.  A work item is up to 128 tokens of
 // one expert times two 128-row weight matrices (gate and up rows j0..j0+127 for
 // stage 4; down rows i0..i0+255 for stage 6); items come from an atomic ticket
 // over the device-built, longest-first work list.  Roles, connected by
 // mbarrier full/empty rings:
-//   scheduler (warp 17): takes tickets, publishes items to a 4-entry ring;
-//   weight converters (warps 8-11): lane = weight row (TMEM lane), per block
-//     the raw row -> binary16 hi and lo of d*q, written to the A stage in TMEM
-//     with tcgen05.st;
-//   token converters (warps 12-15): lane = token, per block the q8_1 row ->
+//   scheduler (warp 21): takes tickets, publishes items to a 4-entry ring;
+//   weight converters (warps 8-15, one per TMEM lane quarter and matrix):
+//     lane = weight row, per block the raw row -> binary16 hi and lo of d*q,
+//     written to the A stage in TMEM with tcgen05.st;
+//   token converters (warps 16-19): lane = token, per block the q8_1 row ->
 //     hi and lo, written to the B stage in shared memory (K-major);
-//   MMA issuer (warp 16): per block 2 matrices x 2 K-steps x 3 terms of
-//     (M=128, N=tokens rounded to 16, K=16) into one 256-column accumulator;
+//   MMA issuers (warp 20 for matrix 0, warp 22 for matrix 1): per block 2
+//     K-steps x 3 terms of (M=128, N=tokens rounded to 16, K=16) into the
+//     matrix's half of one 256-column accumulator; each commits on its own,
+//     the operand, m-term and accumulator barriers count both, and one
+//     issuer's barrier probes and commits overlap the other's MMAs;
 //   epilogue (warps 0-7): once per item, the accumulator -> a shared-memory
 //     staging buffer (the accumulator is released as soon as it is copied),
 //     SiLU(g)*u for stage 4, then one bulk copy per output row.
@@ -64,8 +67,10 @@ constexpr int EPI_WARPS = 8;
 constexpr int WCVT_WARP0 = 8, WCVT_WARPS = 8;    // (lane quarter, matrix)
 constexpr int XCVT_WARP0 = 16, XCVT_WARPS = 4;   // 32 tokens each
 constexpr int CVT_WARPS = WCVT_WARPS + XCVT_WARPS;
-constexpr int MMA_WARP = 20, SCHED_WARP = 21;
-constexpr int THREADS = 22 * 32;
+// two MMA issuers, one per matrix (warps 20 and 22), so that one's barrier
+// probes and commits overlap the other's MMAs
+constexpr int MMA_WARP = 20, SCHED_WARP = 21, MMA_WARP2 = 22, MMA_ISSUERS = 2;
+constexpr int THREADS = 23 * 32;
 
 // tensor memory columns
 constexpr uint32_t T_ACC = 0;                // [matrix][BN token columns]
@@ -273,13 +278,13 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
         }
         for (int i = 0; i < AS; ++i) {
             mbar_init(bar(B_OF + i), CVT_WARPS);
-            mbar_init(bar(B_OE + i), 1);
+            mbar_init(bar(B_OE + i), MMA_ISSUERS);
         }
         for (int i = 0; i < MS; ++i) {
             mbar_init(bar(B_MF + i), CVT_WARPS);
-            mbar_init(bar(B_ME + i), 1);
+            mbar_init(bar(B_ME + i), MMA_ISSUERS);
         }
-        mbar_init(bar(B_AF), 1);
+        mbar_init(bar(B_AF), MMA_ISSUERS);
         mbar_init(bar(B_AE), EPI_WARPS);
         mbar_init(bar(B_EPI), EPI_WARPS);
         *abort_flag = 0;
@@ -601,8 +606,9 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
             }
         }
         if (__any_sync(0xffffffffu, range_bad) && lane == 0) set_error(P.err, MOE_DEV_ERR_RANGE);
-    } else if (warp == MMA_WARP) {
+    } else if (warp == MMA_WARP || warp == MMA_WARP2) {
         if (lane == 0) {
+            const int mat = warp == MMA_WARP ? 0 : 1;  // this issuer's matrix
             // ---- MMA issuer.  A lean loop: operand descriptors advance by
             // constant offsets, and the next block's operand barrier is probed
             // before this block's MMAs are issued, so the probe's latency
@@ -635,8 +641,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
                     ready = b + 1 < nb && mbar_test_wait(bar(B_OF + sn), (phn >> sn) & 1);
                     const uint64_t bd = bdesc0 + (uint64_t)((s * 2 * XT) >> 4);
                     const uint32_t as = a0 + s * 64;
-#pragma unroll
-                    for (int mat = 0; mat < 2; ++mat) {
+                    {
                         const uint32_t d = tmem + T_ACC + mat * BN;
 #pragma unroll
                         for (int ks = 0; ks < 2; ++ks) {
@@ -661,9 +666,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
                         }
                         tc_fence_after();
                         const uint64_t bm = sdesc(sbase + O_BM + ms * BN * 32, 128, 256);
-#pragma unroll
-                        for (int mat = 0; mat < 2; ++mat)
-                            mma_tmem_a(tmem + T_ACC + mat * BN, tmem + T_M + ms * 16 + mat * 8, bm, id, 1u);
+                        mma_tmem_a(tmem + T_ACC + mat * BN, tmem + T_M + ms * 16 + mat * 8, bm, id, 1u);
                         mma_commit(bar(B_ME + ms));
                         last_bar = B_ME + ms;
                         last_par = (cw / MS) & 1;

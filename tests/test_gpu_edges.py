@@ -114,3 +114,30 @@ def test_shape_outside_the_tensor_core_kernel(wtype):
     assert bits == 0
     ref = _oracle(wtype, E, d, f, arena, rb, stride, x, ids, w)
     assert H.rel_l2_rows(out, ref).max() <= 2e-3
+
+
+@pytest.mark.parametrize("wtype,path", [(mw.Q8_0, None), (mw.Q8_0, "simt"), (mw.Q2_K, None)])
+def test_maximum_expert_count(wtype, path, monkeypatch):
+    """E = 8192, the largest expert count the calls accept, with K = 16 routed
+    experts a token: most experts get one or two rows, so every group of 16 and
+    every work item is ragged; every token against the oracle, fused and
+    streamed forms included where the tensor-core kernel runs."""
+    if path:
+        monkeypatch.setenv("MOE_MMQ_PATH", path)
+    E, K, T = 8192, 16, 400
+    d, f = 256, 256 if wtype == mw.Q2_K else 128
+    arena, rb, stride, x, ids, w = _problem(wtype, T, d, f, E, K, 31)
+    x[17] = 0.0
+    out, bits = _run(wtype, E, d, f, arena, rb, stride, x, ids, w)
+    assert bits == 0
+    ref = _oracle(wtype, E, d, f, arena, rb, stride, x, ids, w)
+    assert H.rel_l2_rows(out, ref).max() <= 2e-3
+    assert not out[17].any()
+    if path is None:
+        layer = m.MoeLayer(wtype, E, d, f, K, T, H.to_dev(arena), rb, stride)
+        xd, idd, wd = H.to_dev(x), H.to_dev(ids), H.to_dev(w)
+        fused = layer.forward(xd, idd, wd, fused=True).cpu().numpy()
+        assert m.moe_device_error(layer.ws) == 0
+        assert H.rel_l2_rows(fused, ref).max() <= 2e-3
+        streamed, _ = _run(wtype, E, d, f, arena, rb, stride, x, ids, w, streamed=True)
+        assert np.array_equal(streamed, out)
