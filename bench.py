@@ -246,7 +246,7 @@ PROFILED_TRAFFIC = {
         "code_sha256_16": "31258400117109e3", "bytes": 609559808 + 254505216},
     ("mmq_down", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/mmq_fold.cu",
-        "code_sha256_16": "9f291966bc921c47", "bytes": 275967232 + 666515712},
+        "code_sha256_16": "954cac85112a4529", "bytes": 275706624 + 667205888},
     ("quantize_scatter", "T32768_d2048_f768_E512_K10_q4_1"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/quantize.cu",
         "code_sha256_16": "217e4c4ac0275670", "bytes": 270006272 + 694668800},
