@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -469,6 +470,9 @@ def run_gpu(args, rank, world, local_rank):
         "quantize_scatter": {"GB/s": round(qs_gbs, 1), "frac_of_hbm": round(qs_gbs / hbm, 4),
                              "bytes": int(stages["quantize_scatter"][0])},
         "phases_ms": phases,
+        "phases_median_ms": {n: round(float(v), 4)
+                             for n, v in zip(stage_names, np.median(stage_ms, axis=0))},
+        "ms_per_step_median": round(float(np.median(step_ms)), 4),
         "e2e": {"value": round(weak_scaling_value(world, T, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": int(wl.x.nbytes + wl.ids.nbytes + wl.w.nbytes),
@@ -871,6 +875,44 @@ def time_oracle_threads(wl, n_tokens, threads):
     return time.perf_counter() - t
 
 
+def host_cpu_model() -> str:
+    """The host CPU's name as /proc/cpuinfo gives it (x86 'model name', or the
+    Arm implementer / part numbers), else the machine type."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model"):
+        for line in info.splitlines():
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    impl = part = None
+    for line in info.splitlines():
+        if line.startswith("CPU implementer") and impl is None:
+            impl = line.split(":", 1)[1].strip()
+        if line.startswith("CPU part") and part is None:
+            part = line.split(":", 1)[1].strip()
+    if impl or part:
+        return f"{platform.machine()} implementer {impl} part {part}"
+    return platform.machine()
+
+
+def time_oracle_quantize(wl):
+    """The oracle's stage 2 alone on the whole workload (single-threaded C):
+    GB/s over the stage's algorithmic bytes."""
+    import oracle
+    cfg = wl.cfg
+    sm = oracle.build_slot_map(wl.ids, cfg.E)
+    R = int(sm["offsets"][cfg.E])
+    t = time.perf_counter()
+    oracle.quantize_scatter_q8_1(wl.x, sm["slot"], cfg.K, R, layout=oracle.layout_of(cfg.wtype))
+    sec = time.perf_counter() - t
+    q8 = 1.25 if cfg.wtype == mw.Q2_K else 1.125
+    nbytes = cfg.T * cfg.d * 4 + R * cfg.d * q8 + cfg.T * cfg.K * 4
+    return {"GB/s": round(nbytes / sec / 1e9, 3), "ms": round(sec * 1e3, 2),
+            "sample": f"all {cfg.T} tokens, single-threaded C"}
+
+
 def cpu_baseline(wl, budget_s: float = 15.0):
     n = calibrate_tokens(wl, budget_s)
     sec = time_oracle(wl, n)
@@ -878,7 +920,8 @@ def cpu_baseline(wl, budget_s: float = 15.0):
     out = {"value": round(n / sec, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
            "sample": f"{n} seeded tokens of the {wl.cfg.T}-token workload with their routing "
                      f"(all seven stages, single-threaded C, {sec:.1f} s)",
-           "host_cores": cores}
+           "host_cores": cores, "host_cpu": host_cpu_model(),
+           "quantize_scatter": time_oracle_quantize(wl)}
     if cores > 1:
         # the same oracle functions, one host thread per core over disjoint tokens
         nm = min(wl.cfg.T, n * cores)
