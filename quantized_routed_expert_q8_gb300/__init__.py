@@ -380,6 +380,75 @@ class MoeLayer:
         moe_combine_topk(self.y, R, self.slot, w, T, K, d, self.out, stream)
         return self.out[:T]
 
+    def forward_host(self, hx, hids, hw, hout, chunks=4, stream=None):
+        """As forward, from pinned host inputs hx f32 [T, d], hids i32 [T, K],
+        hw f32 [T, K] to the pinned host output hout f32 [T, d], with the
+        host-device copies overlapped with the layer on a copy stream of the
+        layer's own: ids and w first, then x in `chunks` token slices, each
+        quantized (stage 2 on its tokens) as soon as it has landed while the
+        routing map and the group gather run; at the end the combine (stage 7)
+        runs per token slice and each slice's output is copied back while the
+        next is combined.  The same kernels and bytes as forward.  Returns hout;
+        the copies are complete once `stream` (default: the current stream)
+        reaches the point of return."""
+        T = hx.shape[0]
+        assert T <= self.T_max and hids.shape == (T, self.K) and hw.shape == (T, self.K)
+        assert hout.shape == (T, self.d)
+        dev = self.group_buf.device
+        cs = stream if stream is not None else torch.cuda.current_stream(dev)
+        if not hasattr(self, "host_copy_stream"):
+            self.host_copy_stream = torch.cuda.Stream(device=dev)
+            self.dx = torch.zeros((max(self.T_max, 1), self.d), dtype=torch.float32, device=dev)
+            self.dids = torch.zeros((max(self.T_max, 1), self.K), dtype=torch.int32, device=dev)
+            self.dw = torch.zeros((max(self.T_max, 1), self.K), dtype=torch.float32, device=dev)
+        xs = self.host_copy_stream
+        K, E, d, f = self.K, self.E, self.d, self.f
+        R = T * K
+        n = max(1, min(chunks, T))
+        bounds = [T * i // n for i in range(n + 1)]
+        x_ready = [torch.cuda.Event() for _ in range(n)]
+        routing_ready = torch.cuda.Event()
+        xs.wait_stream(cs)  # the staging buffers' previous readers are done
+        with torch.cuda.stream(xs):
+            self.dids[:T].copy_(hids, non_blocking=True)
+            self.dw[:T].copy_(hw, non_blocking=True)
+            routing_ready.record(xs)
+            for c in range(n):
+                t0, t1 = bounds[c], bounds[c + 1]
+                self.dx[t0:t1].copy_(hx[t0:t1], non_blocking=True)
+                x_ready[c].record(xs)
+        ids, w = self.dids[:T], self.dw[:T]
+        cs.wait_event(routing_ready)
+        moe_build_slot_map(ids, E, self.offsets, self.slot, self.src, self.active, self.n_active,
+                           self.ws, cs)
+        moe_group_gather_active(self.arena, self.rec_bytes, self.arena_stride, self.active,
+                                self.n_active, E, self.group_buf, self.slot_stride, cs)
+        scatter, _, requant = quantizers(self.wtype)
+        for c in range(n):
+            t0, t1 = bounds[c], bounds[c + 1]
+            cs.wait_event(x_ready[c])
+            if t1 > t0:
+                scatter(self.dx[t0:t1], self.slot[t0 * K:t1 * K], K, R, self.q, self.ds, cs)
+        moe_grouped_mmq_gateup(self.wtype, self.group_buf, self.slot_stride, self.active,
+                               self.n_active, self.offsets, E, self.q, self.ds, R, d, f, self.h,
+                               self.ws, cs)
+        requant(self.h, R, f, self.hq, self.hds, cs)
+        moe_grouped_mmq_down(self.wtype, self.group_buf, self.slot_stride, self.active,
+                             self.n_active, self.offsets, E, self.hq, self.hds, R, d, f, self.y,
+                             self.ws, cs)
+        for c in range(n):
+            t0, t1 = bounds[c], bounds[c + 1]
+            if t1 > t0:
+                moe_combine_topk(self.y, R, self.slot[t0 * K:t1 * K], w[t0:t1], t1 - t0, K, d,
+                                 self.out[t0:t1], cs)
+            done = torch.cuda.Event()
+            done.record(cs)
+            xs.wait_event(done)
+            with torch.cuda.stream(xs):
+                hout[t0:t1].copy_(self.out[t0:t1], non_blocking=True)
+        cs.wait_stream(xs)
+        return hout
+
     def forward_streamed(self, host_arena, x, ids, w, ring_groups=3, stream=None):
         """As forward, with the expert records read from host_arena (pinned host
         memory, record e at e*arena_stride) and streamed through a device ring of

@@ -61,3 +61,25 @@ def test_streamed_rejects_bad_arguments():
     with pytest.raises(m.MoeError):
         layer.forward_streamed(host_arena, x, ids, w, ring_groups=65)
     assert np.isfinite(layer.forward_streamed(host_arena, x, ids, w).cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("name,chunks", [(mw.TINY.name, 4), (mw.T600.name, 1), (mw.T600.name, 3),
+                                         (mw.T2048_Q2K.name, 4), (mw.T8192.name, 4)])
+def test_forward_host_equals_forward(name, chunks):
+    """MoeLayer.forward_host (pinned host in, pinned host out, copies overlapped
+    with the layer on a copy stream, stage 2 and stage 7 per token slice) gives
+    the same bytes as forward on device inputs, twice in a row."""
+    wl = H.workload(name)
+    layer = _layer(wl)
+    ref = layer.forward(H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w)).cpu().numpy()
+    assert m.moe_device_error(layer.ws) == 0
+    hx = torch.from_numpy(wl.x).pin_memory()
+    hids = torch.from_numpy(wl.ids).pin_memory()
+    hw = torch.from_numpy(wl.w).pin_memory()
+    for _ in range(2):
+        hout = torch.full((wl.cfg.T, wl.cfg.d), float("nan")).pin_memory()
+        layer.out.fill_(float("nan"))
+        got = layer.forward_host(hx, hids, hw, hout, chunks=chunks)
+        torch.cuda.current_stream().synchronize()
+        assert m.moe_device_error(layer.ws) == 0
+        assert np.array_equal(got.numpy(), ref)
