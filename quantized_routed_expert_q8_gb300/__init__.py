@@ -404,7 +404,8 @@ class MoeLayer:
         xs = self.host_copy_stream
         K, E, d, f = self.K, self.E, self.d, self.f
         R = T * K
-        n = max(1, min(chunks, T))
+        # slices of at least 1 MB of x: below that the copies are too short to hide anything
+        n = max(1, min(chunks, T, T * self.d * 4 // (1 << 20)))
         bounds = [T * i // n for i in range(n + 1)]
         x_ready = [torch.cuda.Event() for _ in range(n)]
         routing_ready = torch.cuda.Event()
