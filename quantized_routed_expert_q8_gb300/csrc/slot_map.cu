@@ -66,13 +66,21 @@ __global__ void __launch_bounds__(1024) slot_scan_kernel(int32_t* __restrict__ c
                                                          int32_t* __restrict__ active,
                                                          int32_t* __restrict__ n_active) {
     extern __shared__ int32_t tot[];  // [E]
-    // per expert: running prefix over chunks (column walk, coalesced across e)
+    // per expert: running prefix over chunks (column walk, coalesced across e),
+    // 8 chunks' counts loaded at once so that their latencies overlap
+    constexpr int CB = 8;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
-        for (int c = 0; c < n_chunks; ++c) {
-            int v = chunk_counts[(size_t)c * E + e];
-            chunk_counts[(size_t)c * E + e] = run;
-            run += v;
+        for (int c0 = 0; c0 < n_chunks; c0 += CB) {
+            int v[CB];
+#pragma unroll
+            for (int j = 0; j < CB; ++j)
+                v[j] = c0 + j < n_chunks ? chunk_counts[(size_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < CB; ++j) {
+                if (c0 + j < n_chunks) chunk_counts[(size_t)(c0 + j) * E + e] = run;
+                run += v[j];
+            }
         }
         tot[e] = run;
     }
@@ -117,10 +125,23 @@ __global__ void __launch_bounds__(32) slot_rank_kernel(const int32_t* __restrict
     __syncwarp();
     int lo = c * SLOT_CHUNK, hi = min(TK, lo + SLOT_CHUNK);
     unsigned lt = (1u << lane) - 1u;
-    for (int i0 = lo; i0 < hi; i0 += 32) {
+    // the ids of 8 steps (256 entries) are loaded at once, so that their
+    // latencies overlap; the steps then run in order
+    constexpr int SB = 8;
+    for (int b0 = lo; b0 < hi; b0 += 32 * SB) {
+      int eb[SB];
+#pragma unroll
+      for (int j = 0; j < SB; ++j) {
+          const int i = b0 + 32 * j + lane;
+          eb[j] = i < hi ? ids[i] : -1;
+      }
+#pragma unroll
+      for (int j = 0; j < SB; ++j) {
+        const int i0 = b0 + 32 * j;
+        if (i0 >= hi) break;  // warp-uniform
         int i = i0 + lane;
         bool in = i < hi;
-        int e = in ? ids[i] : -1;
+        int e = eb[j];
         bool valid = in && (unsigned)e < (unsigned)E;
         int key = valid ? e : E + lane;  // invalid entries match nobody
         unsigned peers = __match_any_sync(0xffffffffu, key);
@@ -133,6 +154,7 @@ __global__ void __launch_bounds__(32) slot_rank_kernel(const int32_t* __restrict
             slot[i] = row;
             if (valid) src[row] = i / K;
         }
+      }
     }
 }
 
