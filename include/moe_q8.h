@@ -190,9 +190,11 @@ int moe_group_gather(const uint8_t* arena, size_t rec_bytes, size_t arena_stride
  * Stage 3 for a whole layer without a host round trip: the groups of 16 active
  * experts (ascending id, as listed by moe_build_slot_map) gathered back to
  * back; the expert at active position p lands at group_base + p*slot_stride.
- * One launch covers every group (blockIdx.y = expert within its group,
- * blockIdx.z = group).  active and n_active are device pointers; max_active
- * bounds n_active (normally E).
+ * One launch covers every group: a persistent grid walks the (routed expert,
+ * 128 KB part of its record) units up to the device-side count, so no block
+ * is spent on an expert that is not routed.  The same bytes as the per-group
+ * calls.  active and n_active are device pointers; max_active bounds n_active
+ * (normally E).
  */
 int moe_group_gather_active(const uint8_t* arena, size_t rec_bytes, size_t arena_stride,
                             const int32_t* active, const int32_t* n_active, int max_active,

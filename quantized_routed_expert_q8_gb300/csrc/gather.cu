@@ -49,20 +49,48 @@ __global__ void __launch_bounds__(256) group_gather_kernel(const uint8_t* __rest
     else copy_bytes(s, dd, rec_bytes);
 }
 
+// The whole layer's groups in one launch: a persistent grid walks the units
+// (active position p, 128 KB part of its record) up to the device-side count, so
+// that no block is launched for an expert that is not routed.
+constexpr size_t PART = 128u << 10;  // bytes of a record one unit copies
+
+__device__ __forceinline__ void copy_range_vec(const uint4* __restrict__ src,
+                                               uint4* __restrict__ dst, size_t n16) {
+    size_t i = threadIdx.x;
+    const size_t st = blockDim.x;
+    for (; i + 3 * st < n16; i += 4 * st) {
+        uint4 a = __ldcs(src + i), b = __ldcs(src + i + st), c = __ldcs(src + i + 2 * st),
+              d = __ldcs(src + i + 3 * st);
+        dst[i] = a;
+        dst[i + st] = b;
+        dst[i + 2 * st] = c;
+        dst[i + 3 * st] = d;
+    }
+    for (; i < n16; i += st) dst[i] = __ldcs(src + i);
+}
+
 template <bool VEC>
-__global__ void __launch_bounds__(256) group_gather_active_kernel(
+__global__ void __launch_bounds__(256, 8) group_gather_active_kernel(
     const uint8_t* __restrict__ arena, size_t rec_bytes, size_t arena_stride,
     const int32_t* __restrict__ active, const int32_t* __restrict__ n_active, int max_active,
     uint8_t* __restrict__ base, size_t slot_stride) {
-    int p = blockIdx.z * 16 + blockIdx.y;  // active position: group z, slot y
-    int n = min(*n_active, max_active);
-    if (p >= n) return;
-    int e = active[p];
-    if (e < 0) return;
-    const uint8_t* s = arena + (size_t)e * arena_stride;
-    uint8_t* dd = base + (size_t)p * slot_stride;
-    if (VEC) copy_vec(reinterpret_cast<const uint4*>(s), reinterpret_cast<uint4*>(dd), rec_bytes / 16);
-    else copy_bytes(s, dd, rec_bytes);
+    const int n = min(*n_active, max_active);
+    const long long parts = (long long)((rec_bytes + PART - 1) / PART);
+    const long long units = (long long)n * parts;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+        const int p = (int)(u / parts);  // active position
+        const size_t off = (size_t)(u % parts) * PART;
+        const size_t len = rec_bytes - off < PART ? rec_bytes - off : PART;
+        const int e = active[p];
+        if (e < 0) continue;
+        const uint8_t* s = arena + (size_t)e * arena_stride + off;
+        uint8_t* dd = base + (size_t)p * slot_stride + off;
+        if (VEC) {
+            copy_range_vec(reinterpret_cast<const uint4*>(s), reinterpret_cast<uint4*>(dd), len / 16);
+        } else {
+            for (size_t i = threadIdx.x; i < len; i += blockDim.x) dd[i] = s[i];
+        }
+    }
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
@@ -98,7 +126,11 @@ int launch_group_gather_active(const uint8_t* arena, size_t rec_bytes, size_t ar
     if (rec_bytes == 0 || max_active <= 0) return MOE_OK;
     bool vec = aligned16(arena) && aligned16(base) && rec_bytes % 16 == 0 &&
                arena_stride % 16 == 0 && slot_stride % 16 == 0;
-    dim3 grid(blocks_per_record(rec_bytes), 16, (max_active + 15) / 16);
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long units = (long long)max_active * (long long)((rec_bytes + PART - 1) / PART);
+    const int grid = (int)(units < (long long)sms * 8 ? units : (long long)sms * 8);  // 8 blocks an SM
     if (vec)
         group_gather_active_kernel<true><<<grid, 256, 0, stream>>>(
             arena, rec_bytes, arena_stride, active, n_active, max_active, base, slot_stride);
