@@ -214,6 +214,10 @@ struct Params {
     const float* wts;       // [T*K] top-k weights
     int32_t* arrivals;      // [T][d/256] rows of the token still to be written
     int K, T;
+    // failure-detection test hook: CTA 0 withholds the partials commit of its
+    // block stall_idx, so its epilogue's bounded wait runs out (MOE_DEV_ERR_TIMEOUT)
+    // and every role exits; -1 (the default) withholds nothing
+    int stall_idx;
 };
 
 struct Item {
@@ -835,7 +839,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 sdesc(fbB + k16 * 256, 128, 512), id, (uint32_t)k16);
                     }
                 }
-                mma_commit(bar(B_TM_FULL + tb));
+                if (!(idx == P.stall_idx && blockIdx.x == 0)) mma_commit(bar(B_TM_FULL + tb));
                 mma_commit(bar(B_F16_EMPTY + fs));
             }
             // the last committed group must land before TMEM is freed
@@ -878,6 +882,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool debug() {
     static const bool on = std::getenv("MOE_DEBUG") != nullptr;
     return on;
+}
+
+// MOE_TEST_STALL_BLOCK=n: the failure-detection test's hook (Params::stall_idx);
+// read at every launch so that a test can set and clear it
+int test_stall_idx() {
+    const char* v = std::getenv("MOE_TEST_STALL_BLOCK");
+    return v ? std::atoi(v) : -1;
 }
 
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
@@ -1058,6 +1069,7 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     P.arrivals = F.arrivals;
     P.K = F.K;
     P.T = F.T;
+    P.stall_idx = test_stall_idx();
     long long upper = ((long long)R / BN + E + 1) * P.mt_count;
     int grid = (int)(upper < sms ? upper : sms);
     mmq_tc_kernel<WT, GU, FUSED><<<grid, THREADS, L::SMEM, stream>>>(mW, mWs, mWm, mWc, mX, mXs, P);

@@ -141,3 +141,34 @@ def test_maximum_expert_count(wtype, path, monkeypatch):
         assert H.rel_l2_rows(fused, ref).max() <= 2e-3
         streamed, _ = _run(wtype, E, d, f, arena, rb, stride, x, ids, w, streamed=True)
         assert np.array_equal(streamed, out)
+
+
+def test_bounded_wait_reports_timeout(monkeypatch):
+    """Failure detection without a fault: MOE_TEST_STALL_BLOCK makes CTA 0 of the
+    per-block-scaling MMQ withhold one partials commit, so its epilogue's
+    bounded wait runs out (about 2 s); the kernel sets MOE_DEV_ERR_TIMEOUT, every
+    role exits, and the context stays usable: the next call is exact again."""
+    wl = H.workload(mw.TINY.name)
+    cfg = wl.cfg
+    layer = m.MoeLayer(cfg.wtype, cfg.E, cfg.d, cfg.f, cfg.K, cfg.T, H.to_dev(wl.arena),
+                       wl.rec_bytes, wl.arena_stride)
+    x, ids, w = H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w)
+    ref = layer.forward(x, ids, w).cpu().numpy()
+    assert m.moe_device_error(layer.ws) == 0
+    R = cfg.T * cfg.K
+
+    def gateup():
+        m.moe_grouped_mmq_gateup(layer.wtype, layer.group_buf, layer.slot_stride, layer.active,
+                                 layer.n_active, layer.offsets, cfg.E, layer.q, layer.ds, R, cfg.d,
+                                 cfg.f, layer.h, layer.ws)
+
+    monkeypatch.setenv("MOE_TEST_STALL_BLOCK", "3")
+    gateup()
+    bits = m.moe_device_error(layer.ws)
+    assert bits & m.DEV_ERR_TIMEOUT
+    monkeypatch.delenv("MOE_TEST_STALL_BLOCK")
+    gateup()
+    assert m.moe_device_error(layer.ws) == 0
+    out = layer.forward(x, ids, w).cpu().numpy()
+    assert m.moe_device_error(layer.ws) == 0
+    assert np.array_equal(out, ref)
