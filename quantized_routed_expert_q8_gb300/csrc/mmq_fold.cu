@@ -120,6 +120,10 @@ struct Params {
     const uint32_t* xds; // [R][nb] (d, s) binary16 pairs
     float* out;          // [R][n_out]
     uint32_t* err;
+    // failure-detection test hook: CTA 0's matrix-0 issuer withholds the
+    // operand-release commit of its block stall_idx, so the converters' bounded
+    // wait for that stage runs out (MOE_DEV_ERR_TIMEOUT); -1 withholds nothing
+    int stall_idx;
 };
 
 // ---------------------------------------------------------------- device ---
@@ -620,6 +624,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
             uint32_t ph = 0;    // bit k: phase parity of stage k's next fill
             int last_bar = -1;
             uint32_t last_par = 0;
+            int gblk = 0;  // blocks issued by this thread so far
             for (int i = 0;; ++i) {
                 if (!mbar_wait(bar(B_IF + i % IR), (i / IR) & 1, abort_flag)) break;
                 const int4 e = ring[i % IR];
@@ -630,7 +635,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
                 tc_fence_after();
                 bool ready = mbar_test_wait(bar(B_OF + s), (ph >> s) & 1);
                 bool ok = true;
-                for (int b = 0; b < nb; ++b) {
+                for (int b = 0; b < nb; ++b, ++gblk) {
                     if (!ready && !mbar_wait(bar(B_OF + s), (ph >> s) & 1, abort_flag)) {
                         ok = false;
                         break;
@@ -653,7 +658,8 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
                             mma_tmem_a(d, ah, bl, id, 1u);
                         }
                     }
-                    mma_commit(bar(B_OE + s));
+                    if (!(gblk == P.stall_idx && blockIdx.x == 0 && mat == 0))
+                        mma_commit(bar(B_OE + s));
                     last_bar = B_OE + s;
                     last_par = (ph >> s) & 1;
                     ph = phn;
@@ -679,8 +685,10 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
             // everything committed must land before TMEM is freed
             if (last_bar >= 0) {
                 long long t0 = clock64();
-                while (!mbar_try_wait(bar(last_bar), last_par) && clock64() - t0 < TIMEOUT_CYCLES) {
+                bool landed = false;
+                while (!(landed = mbar_try_wait(bar(last_bar), last_par)) && clock64() - t0 < TIMEOUT_CYCLES) {
                 }
+                if (!landed) *abort_flag = 1;  // reported as MOE_DEV_ERR_TIMEOUT
             }
         }
     } else if (warp < EPI_WARPS) {
@@ -809,6 +817,10 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     int32_t* counters = (int32_t*)(ws + W.counters);
     P.n_tiles = counters + MMQ_COUNTER_NTILES;
     P.ticket = counters + MMQ_COUNTER_TICKET;
+    {
+        const char* v = std::getenv("MOE_TEST_STALL_BLOCK");  // the test hook, read per launch
+        P.stall_idx = v ? std::atoi(v) : -1;
+    }
     P.mt_count = GU ? f / BM : d / (2 * BM);
     P.nb = P.klen / QK;
     P.n_out = GU ? f : d;

@@ -806,9 +806,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             // only on the abort path)
             for (int g = (gs > RS ? gs - RS : 0); g < gs; ++g) {
                 long long t0 = clock64();
-                while (!mbar_try_wait(bar(B_RAW_FULL + g % RS), (g / RS) & 1) &&
+                bool landed = false;
+                while (!(landed = mbar_try_wait(bar(B_RAW_FULL + g % RS), (g / RS) & 1)) &&
                        clock64() - t0 < TIMEOUT_CYCLES) {
                 }
+                if (!landed) *abort_flag = 1;  // reported as MOE_DEV_ERR_TIMEOUT
             }
         } else if (warp == EPI_WARPS + CVT_WARPS + 1 && lane == 0) {
             // ---- MMA issuer: block idx's products into TMEM buffer idx % NTB,
@@ -846,9 +848,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (idx > 0) {
                 const int last = idx - 1;
                 long long t0 = clock64();
-                while (!mbar_try_wait(bar(B_TM_FULL + last % NTB), (last / NTB) & 1) &&
+                bool landed = false;
+                while (!(landed = mbar_try_wait(bar(B_TM_FULL + last % NTB), (last / NTB) & 1)) &&
                        clock64() - t0 < TIMEOUT_CYCLES) {
                 }
+                if (!landed) *abort_flag = 1;  // reported as MOE_DEV_ERR_TIMEOUT
             }
         }
     }

@@ -144,10 +144,11 @@ def test_maximum_expert_count(wtype, path, monkeypatch):
 
 
 def test_bounded_wait_reports_timeout(monkeypatch):
-    """Failure detection without a fault: MOE_TEST_STALL_BLOCK makes CTA 0 of the
-    per-block-scaling MMQ withhold one partials commit, so its epilogue's
-    bounded wait runs out (about 2 s); the kernel sets MOE_DEV_ERR_TIMEOUT, every
-    role exits, and the context stays usable: the next call is exact again."""
+    """Failure detection without a fault: MOE_TEST_STALL_BLOCK makes CTA 0 of
+    the per-block-scaling MMQ (stage 4) withhold one partials commit and CTA 0 of
+    the folded-scale MMQ (stage 6) one operand-release commit, so a bounded wait
+    runs out (about 2 s); the kernel sets MOE_DEV_ERR_TIMEOUT, every role exits,
+    and the context stays usable: the next calls are exact again."""
     wl = H.workload(mw.TINY.name)
     cfg = wl.cfg
     layer = m.MoeLayer(cfg.wtype, cfg.E, cfg.d, cfg.f, cfg.K, cfg.T, H.to_dev(wl.arena),
@@ -162,13 +163,19 @@ def test_bounded_wait_reports_timeout(monkeypatch):
                                  layer.n_active, layer.offsets, cfg.E, layer.q, layer.ds, R, cfg.d,
                                  cfg.f, layer.h, layer.ws)
 
-    monkeypatch.setenv("MOE_TEST_STALL_BLOCK", "3")
-    gateup()
-    bits = m.moe_device_error(layer.ws)
-    assert bits & m.DEV_ERR_TIMEOUT
-    monkeypatch.delenv("MOE_TEST_STALL_BLOCK")
-    gateup()
-    assert m.moe_device_error(layer.ws) == 0
+    def down():  # the folded-scale kernel: an operand-release commit withheld
+        m.moe_grouped_mmq_down(layer.wtype, layer.group_buf, layer.slot_stride, layer.active,
+                               layer.n_active, layer.offsets, cfg.E, layer.hq, layer.hds, R, cfg.d,
+                               cfg.f, layer.y, layer.ws)
+
+    for call in (gateup, down):
+        monkeypatch.setenv("MOE_TEST_STALL_BLOCK", "0")
+        call()
+        bits = m.moe_device_error(layer.ws)
+        assert bits & m.DEV_ERR_TIMEOUT, call.__name__
+        monkeypatch.delenv("MOE_TEST_STALL_BLOCK")
+        call()
+        assert m.moe_device_error(layer.ws) == 0
     out = layer.forward(x, ids, w).cpu().numpy()
     assert m.moe_device_error(layer.ws) == 0
     assert np.array_equal(out, ref)
