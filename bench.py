@@ -244,10 +244,10 @@ def alu_partials(cfg, R: int) -> float:
 PROFILED_TRAFFIC = {
     ("mmq_gateup", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/mmq_tc.cu",
-        "code_sha256_16": "31258400117109e3", "bytes": 609559808 + 254505216},
+        "code_sha256_16": "a3765f4cd7855d9f", "bytes": 609651200 + 254658304},
     ("mmq_down", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/mmq_fold.cu",
-        "code_sha256_16": "954cac85112a4529", "bytes": 275706624 + 667205888},
+        "code_sha256_16": "92e5b88589c25a62", "bytes": 275763200 + 667117824},
     ("quantize_scatter", "T32768_d2048_f768_E512_K10_q4_1"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/quantize.cu",
         "code_sha256_16": "217e4c4ac0275670", "bytes": 270006272 + 694668800},
