@@ -51,6 +51,19 @@ def test_record_bytes_agree(lib, wtype):
     assert m.moe_expert_record_bytes(wtype, 100, 64) == 0  # d not a multiple of 32
 
 
+def test_record_bytes_agree_q2_k(lib):
+    """Q2_K records (super-blocks of 256) agree across the library, the oracle
+    and the generator; widths that are not whole super-blocks are refused."""
+    import quantized_routed_expert_q8_gb300 as m
+    for d, f in ((256, 256), (2048, 768), (512, 1280)):
+        assert m.moe_expert_record_bytes(3, d, f) == oracle.expert_record_bytes(3, d, f)
+        assert m.moe_expert_record_bytes(3, d, f) == mw.record_bytes(3, d, f)
+        assert m.moe_expert_record_offsets(3, d, f) == oracle.record_offsets(3, d, f)
+    assert m.moe_expert_record_bytes(3, 2048, 640) == 0  # f not a multiple of 256
+    assert m.moe_expert_record_bytes(3, 96, 256) == 0
+    assert m.ds_halves(3) == 4 and m.ds_halves(0) == 2
+
+
 def test_status_strings(lib):
     import quantized_routed_expert_q8_gb300 as m
     L = m.lib()
@@ -103,6 +116,13 @@ def test_host_checks_reject_before_launch(lib):
     assert L.moe_grouped_mmq_gateup(0, P(128), 100, P(16), P(16), P(16), 4, P(16), P(16), 8, 64,
                                     64, P(16), P(256), 1 << 20, None) == -2
     assert L.moe_combine_topk(P(16), 8, P(16), P(16), 2, 2, 6, P(16), None) == -1
+    # D2S6 rows: 8-byte (d, s, s_lo, s_hi) entries
+    assert L.moe_quantize_scatter_q8_1_d2s6(P(16), 4, 64, 2, P(16), 8, P(16), P(4), None) == -2
+    assert L.moe_requant_hidden_q8_1_d2s6(P(16), 4, 64, P(16), P(4), None) == -2
+    assert L.moe_quantize_gather_q8_1_d2s6(P(16), 4, 64, P(16), 8, P(16), P(4), None) == -2
+    # Q2_K reductions must be whole 256-weight super-blocks
+    assert L.moe_grouped_mmq_down(3, P(128), 128, P(16), P(16), P(16), 4, P(16), P(16), 8, 256,
+                                  128, P(16), P(256), 1 << 20, None) == -1
 
 
 def test_fused_calls_reject_before_launch(lib):

@@ -22,3 +22,23 @@ def test_alu_partials_counts_every_block_scale():
     R = cfg.T * cfg.K
     want = R * 2 * cfg.f * (cfg.d // 32) + R * cfg.d * (cfg.f // 32)
     assert bench.alu_partials(cfg, R) == want
+
+
+def test_profiled_traffic_entries_name_real_sources():
+    import os
+    for (stage, workload), rec in bench.PROFILED_TRAFFIC.items():
+        assert workload in mw.CONFIGS, workload
+        assert os.path.exists(os.path.join(bench.ROOT, rec["source"])), rec["source"]
+        assert len(rec["code_sha256_16"]) == 16 and rec["bytes"] > 0
+
+
+def test_layer_accounting_q8_1_bytes_per_layout():
+    """Activations cost 1.125 bytes a value in the (d, s) layout and 1.25 in D2S6
+    (Q2_K): the quantize-scatter bytes differ by exactly R*d*0.125."""
+    acc = {}
+    for cfg in (mw.T2048_Q2, mw.T2048_Q2K):
+        R = cfg.T * cfg.K
+        stages, _, _ = bench.layer_accounting(cfg, 512, 1 << 20, R)
+        acc[cfg.wtype] = stages["quantize_scatter"][0]
+    cfg = mw.T2048_Q2K
+    assert acc[mw.Q2_K] - acc[mw.Q2_0] == cfg.T * cfg.K * cfg.d * 0.125
