@@ -380,28 +380,46 @@ class MoeLayer:
         moe_combine_topk(self.y, R, self.slot, w, T, K, d, self.out, stream)
         return self.out[:T]
 
-    def forward_host(self, hx, hids, hw, hout, chunks=4, stream=None):
+    def forward_host(self, hx, hids, hw, hout, chunks=4, stream=None, wait=True):
         """As forward, from pinned host inputs hx f32 [T, d], hids i32 [T, K],
         hw f32 [T, K] to the pinned host output hout f32 [T, d], with the
-        host-device copies overlapped with the layer on a copy stream of the
-        layer's own: ids and w first, then x in `chunks` token slices, each
-        quantized (stage 2 on its tokens) as soon as it has landed while the
-        routing map and the group gather run; at the end the combine (stage 7)
-        runs per token slice and each slice's output is copied back while the
-        next is combined.  The same kernels and bytes as forward.  Returns hout;
-        the copies are complete once `stream` (default: the current stream)
-        reaches the point of return."""
+        host-device copies overlapped with the layer: an upload stream copies ids
+        and w first, then x in `chunks` token slices, each quantized (stage 2 on
+        its tokens) as soon as it has landed while the routing map and the group
+        gather run; at the end the combine (stage 7) runs per token slice and a
+        download stream copies each slice's output back while the next is
+        combined.  The same kernels and bytes as forward.
+
+        The device staging of x, ids and w is double-buffered, so the next call's
+        uploads may run during this call's layer, and this call's downloads
+        during the next call's layer.  wait=True (default): `stream` (default:
+        the current stream) waits for the downloads, so hout is complete once
+        the stream reaches the point of return.  wait=False: it does not, and
+        the returned event marks hout complete -- calls made back to back then
+        overlap one call's copies with another's layer.  Returns that event.
+        The uploads start at once, ordered only after the layer that last read
+        their staging set: hx, hids and hw must hold their values when the call
+        is made (a device-to-host copy that fills them must have completed)."""
         T = hx.shape[0]
         assert T <= self.T_max and hids.shape == (T, self.K) and hw.shape == (T, self.K)
         assert hout.shape == (T, self.d)
         dev = self.group_buf.device
         cs = stream if stream is not None else torch.cuda.current_stream(dev)
-        if not hasattr(self, "host_copy_stream"):
-            self.host_copy_stream = torch.cuda.Stream(device=dev)
-            self.dx = torch.zeros((max(self.T_max, 1), self.d), dtype=torch.float32, device=dev)
-            self.dids = torch.zeros((max(self.T_max, 1), self.K), dtype=torch.int32, device=dev)
-            self.dw = torch.zeros((max(self.T_max, 1), self.K), dtype=torch.float32, device=dev)
-        xs = self.host_copy_stream
+        if not hasattr(self, "_h2d"):
+            self._h2d = torch.cuda.Stream(device=dev)
+            self._d2h = torch.cuda.Stream(device=dev)
+            tm = max(self.T_max, 1)
+            self._staging = [
+                {"x": torch.zeros((tm, self.d), dtype=torch.float32, device=dev),
+                 "ids": torch.zeros((tm, self.K), dtype=torch.int32, device=dev),
+                 "w": torch.zeros((tm, self.K), dtype=torch.float32, device=dev),
+                 "free": None}
+                for _ in range(2)]
+            self._flip = 0
+            self._out_free = None
+        st = self._staging[self._flip]
+        self._flip ^= 1
+        up, dn = self._h2d, self._d2h
         K, E, d, f = self.K, self.E, self.d, self.f
         R = T * K
         # slices of at least 1 MB of x: below that the copies are too short to hide anything
@@ -409,16 +427,18 @@ class MoeLayer:
         bounds = [T * i // n for i in range(n + 1)]
         x_ready = [torch.cuda.Event() for _ in range(n)]
         routing_ready = torch.cuda.Event()
-        xs.wait_stream(cs)  # the staging buffers' previous readers are done
-        with torch.cuda.stream(xs):
-            self.dids[:T].copy_(hids, non_blocking=True)
-            self.dw[:T].copy_(hw, non_blocking=True)
-            routing_ready.record(xs)
+        if st["free"] is not None:
+            up.wait_event(st["free"])  # the layer that last read this staging set is done
+        dx, dids, dw = st["x"], st["ids"], st["w"]
+        with torch.cuda.stream(up):
+            dids[:T].copy_(hids, non_blocking=True)
+            dw[:T].copy_(hw, non_blocking=True)
+            routing_ready.record(up)
             for c in range(n):
                 t0, t1 = bounds[c], bounds[c + 1]
-                self.dx[t0:t1].copy_(hx[t0:t1], non_blocking=True)
-                x_ready[c].record(xs)
-        ids, w = self.dids[:T], self.dw[:T]
+                dx[t0:t1].copy_(hx[t0:t1], non_blocking=True)
+                x_ready[c].record(up)
+        ids, w = dids[:T], dw[:T]
         cs.wait_event(routing_ready)
         moe_build_slot_map(ids, E, self.offsets, self.slot, self.src, self.active, self.n_active,
                            self.ws, cs)
@@ -429,7 +449,7 @@ class MoeLayer:
             t0, t1 = bounds[c], bounds[c + 1]
             cs.wait_event(x_ready[c])
             if t1 > t0:
-                scatter(self.dx[t0:t1], self.slot[t0 * K:t1 * K], K, R, self.q, self.ds, cs)
+                scatter(dx[t0:t1], self.slot[t0 * K:t1 * K], K, R, self.q, self.ds, cs)
         moe_grouped_mmq_gateup(self.wtype, self.group_buf, self.slot_stride, self.active,
                                self.n_active, self.offsets, E, self.q, self.ds, R, d, f, self.h,
                                self.ws, cs)
@@ -437,18 +457,26 @@ class MoeLayer:
         moe_grouped_mmq_down(self.wtype, self.group_buf, self.slot_stride, self.active,
                              self.n_active, self.offsets, E, self.hq, self.hds, R, d, f, self.y,
                              self.ws, cs)
+        if self._out_free is not None:
+            cs.wait_event(self._out_free)  # the previous call's downloads have read out
         for c in range(n):
             t0, t1 = bounds[c], bounds[c + 1]
             if t1 > t0:
                 moe_combine_topk(self.y, R, self.slot[t0 * K:t1 * K], w[t0:t1], t1 - t0, K, d,
                                  self.out[t0:t1], cs)
-            done = torch.cuda.Event()
-            done.record(cs)
-            xs.wait_event(done)
-            with torch.cuda.stream(xs):
+            combined = torch.cuda.Event()
+            combined.record(cs)
+            dn.wait_event(combined)
+            with torch.cuda.stream(dn):
                 hout[t0:t1].copy_(self.out[t0:t1], non_blocking=True)
-        cs.wait_stream(xs)
-        return hout
+        st["free"] = torch.cuda.Event()
+        st["free"].record(cs)  # the combine was this staging set's last reader
+        done = torch.cuda.Event()
+        done.record(dn)
+        self._out_free = done
+        if wait:
+            cs.wait_event(done)
+        return done
 
     def forward_streamed(self, host_arena, x, ids, w, ring_groups=3, stream=None):
         """As forward, with the expert records read from host_arena (pinned host

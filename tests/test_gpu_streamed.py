@@ -79,7 +79,40 @@ def test_forward_host_equals_forward(name, chunks):
     for _ in range(2):
         hout = torch.full((wl.cfg.T, wl.cfg.d), float("nan")).pin_memory()
         layer.out.fill_(float("nan"))
-        got = layer.forward_host(hx, hids, hw, hout, chunks=chunks)
+        layer.forward_host(hx, hids, hw, hout, chunks=chunks)
         torch.cuda.current_stream().synchronize()
         assert m.moe_device_error(layer.ws) == 0
-        assert np.array_equal(got.numpy(), ref)
+        assert np.array_equal(hout.numpy(), ref)
+
+
+@pytest.mark.parametrize("name", [mw.T600.name, mw.T8192.name])
+def test_forward_host_back_to_back(name):
+    """Three forward_host calls on different inputs queued back to back without
+    waiting (wait=False): the double-buffered staging and the output buffer are
+    reused across calls whose copies overlap one another's layers, and every
+    call must still give forward's bytes for its own inputs."""
+    wl = H.workload(name)
+    cfg = wl.cfg
+    layer = _layer(wl)
+    rev = np.ascontiguousarray
+    inputs = [(wl.x, wl.ids, wl.w),
+              (rev(wl.x[::-1]), rev(wl.ids[::-1]), rev(wl.w[::-1])),
+              ((wl.x * np.float32(0.5)).astype(np.float32), rev(np.roll(wl.ids, 1, axis=1)),
+               wl.w)]
+    refs = []
+    for x, ids, w in inputs:
+        refs.append(layer.forward(H.to_dev(x), H.to_dev(ids), H.to_dev(w)).cpu().numpy())
+        assert m.moe_device_error(layer.ws) == 0
+    assert not np.array_equal(refs[0], refs[1]) and not np.array_equal(refs[0], refs[2])
+    host = [tuple(torch.from_numpy(a).pin_memory() for a in inp) for inp in inputs]
+    outs = [torch.full((cfg.T, cfg.d), float("nan")).pin_memory() for _ in inputs]
+    for _ in range(2):
+        for o in outs:
+            o.fill_(float("nan"))
+        events = [layer.forward_host(hx, hids, hw, o, wait=False)
+                  for (hx, hids, hw), o in zip(host, outs)]
+        for ev, o, ref in zip(events, outs, refs):
+            ev.synchronize()
+            assert np.array_equal(o.numpy(), ref)
+        torch.cuda.current_stream().synchronize()
+        assert m.moe_device_error(layer.ws) == 0
