@@ -639,10 +639,9 @@ def streamed_measure(m, layer, wl, x, ids, w, flush, args, resident_ms, n_active
 
 def fused_compare(m, layer, x, ids, w, flush, reps: int = 10):
     """The fused epilogues against the seven calls: the whole layer each way,
-    and each fused call against the two calls it replaces.  The fused calls
-    extend the per-block-scaling kernel, so the byte comparison runs the seven
-    calls on that kernel too (MOE_MMQ_PATH=blockscale); the timings use the
-    default kernels."""
+    and each fused call against the two calls it replaces.  Each fused call runs
+    on the kernel its two calls use by default (gate/up: per-block scaling;
+    down: folded scales), so the layer's bytes must not change."""
     import torch
 
     L = layer
@@ -665,16 +664,6 @@ def fused_compare(m, layer, x, ids, w, flush, reps: int = 10):
         return tot / reps
 
     t_layer = timed(lambda: L.forward(x, ids, w))
-    old_path = os.environ.get("MOE_MMQ_PATH")
-    os.environ["MOE_MMQ_PATH"] = "blockscale"
-    try:
-        L.forward(x, ids, w)
-        torch.cuda.synchronize()
-    finally:
-        if old_path is None:
-            os.environ.pop("MOE_MMQ_PATH", None)
-        else:
-            os.environ["MOE_MMQ_PATH"] = old_path
     ref = L.out[:T].clone()
     hq_ref, y_ref = L.hq.clone(), L.y.clone()
     t_layer_f = timed(lambda: L.forward(x, ids, w, fused=True))

@@ -97,14 +97,17 @@ int mmq_common(int wtype, bool gateup, const uint8_t* group_base, size_t slot_st
     int rc = check_ws(ws, ws_bytes, W.core > ws_need ? W.core : ws_need);
     if (rc) return rc;
     const bool tc = !force_simt() && mmq_tc_supported(wtype, gateup, d, f);
-    if (F && !tc) return MOE_ERR_UNSUPPORTED;
-    const bool fold = !F && !force_simt() && !mmq_path_is("blockscale") &&
-                      (!gateup || mmq_path_is("fold")) && mmq_fold_supported(wtype, d, f);
+    // the folded-scale kernel takes the down projection's combine, not the
+    // gate/up re-quantization
+    const bool fold = (!F || (!gateup && F->comb && !F->hq)) && !force_simt() &&
+                      !mmq_path_is("blockscale") && (!gateup || mmq_path_is("fold")) &&
+                      mmq_fold_supported(wtype, d, f);
+    if (F && !tc && !fold) return MOE_ERR_UNSUPPORTED;
     if (R == 0) return MOE_OK;
     uint8_t* w8 = (uint8_t*)ws;
     if (fold)
         return launch_mmq_fold(wtype, gateup, group_base, slot_stride, active, n_active, offsets,
-                               E, xq, xds, R, d, f, out, w8, W, S(stream));
+                               E, xq, xds, R, d, f, out, w8, W, F ? *F : MmqFused{}, S(stream));
     if (tc)
         return launch_mmq_tc(wtype, gateup, group_base, slot_stride, active, n_active, offsets, E,
                              xq, xds, R, d, f, out, w8, W, F ? *F : MmqFused{}, S(stream));

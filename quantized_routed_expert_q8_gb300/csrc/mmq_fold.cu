@@ -89,7 +89,9 @@ constexpr int B_IF = 0, B_IE = IR, B_OF = 2 * IR, B_OE = B_OF + AS, B_MF = B_OE 
               B_ME = B_MF + MS, B_AF = B_ME + MS, B_AE = B_AF + 1, B_EPI = B_AE + 1,
               N_BARS = B_EPI + 1;
 constexpr int O_RING = O_BAR + ((N_BARS * 8 + 16 + 15) / 16) * 16;
-constexpr int SMEM = O_RING + IR * 16 + 1024;  // + alignment slack
+// down with the combine: [0] count, [1..BN] tokens whose rows are all written
+constexpr int O_LIST = O_RING + IR * 16;
+constexpr int SMEM = O_LIST + (BN + 1) * 4 + 1024;  // + alignment slack
 static_assert(SMEM <= 232448, "shared memory per block");
 
 // binary16 |d| at or above which d*q_max reaches 65520 (overflows binary16)
@@ -120,6 +122,15 @@ struct Params {
     const uint32_t* xds; // [R][nb] (d, s) binary16 pairs
     float* out;          // [R][n_out]
     uint32_t* err;
+    // down with the top-k combine: the combined output, the row -> token and
+    // token -> row maps, the top-k weights, and the count of rows still to be
+    // written for each (token, 256-column block)
+    float* comb;           // [T][n_out]
+    const int32_t* src;    // [R]
+    const int32_t* slot;   // [T*K]
+    const float* wts;      // [T*K]
+    int32_t* arrivals;     // [T][n_out/256]
+    int K, T, R;
     // failure-detection test hook: CTA 0's matrix-0 issuer withholds the
     // operand-release commit of its block stall_idx, so the converters' bounded
     // wait for that stage runs out (MOE_DEV_ERR_TIMEOUT); -1 withholds nothing
@@ -261,7 +272,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t b, uint32_t parity, volatile 
     return __all_sync(0xffffffffu, done);
 }
 
-template <int WT, bool GU>
+template <int WT, bool GU, bool CMB>
 __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -291,6 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
         mbar_init(bar(B_AF), MMA_ISSUERS);
         mbar_init(bar(B_AE), EPI_WARPS);
         mbar_init(bar(B_EPI), EPI_WARPS);
+        *(int*)(smem + O_LIST) = 0;
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -735,17 +747,69 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
                 for (int n = t >> 7; n < rows; n += 2)
                     st[n * STAGE_W + j] = silu_mul(st[n * STAGE_W + j], st[n * STAGE_W + BM + j]);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (!epi_sync()) break;
-            if (warp == 0) {
-                const uint32_t bytes = (GU ? BM : 2 * BM) * 4;
-                for (int n = lane; n < rows; n += 32)
-                    bulk_s2g(P.out + (size_t)(e.y + n) * P.n_out + e.w,
-                             smem_u32(st + n * STAGE_W), bytes);
-                bulk_commit();
-                bulk_wait_read0();
+            if constexpr (CMB) {
+                // Down with the top-k combine ("#1282 ...", "What it does"): the y
+                // rows by generic 16-byte stores, then every row counts down its
+                // (token, 256-column block); the item that writes a token's last
+                // row combines it,
+                //   out[t, c] = fma chain over k ascending of w[t*K+k] * y[slot[t*K+k], c],
+                // the stand-alone combine's arithmetic, whichever item comes last.
+                if (!epi_sync()) break;
+                const int t = threadIdx.x;  // 0..255
+                const int c4 = t & 63;      // 16-byte column of the item's 256 columns
+                for (int n = t >> 6; n < rows; n += EPI_WARPS * 32 / 64)
+                    reinterpret_cast<float4*>(P.out + (size_t)(e.y + n) * P.n_out + e.w)[c4] =
+                        reinterpret_cast<const float4*>(st + n * STAGE_W)[c4];
+                __threadfence();  // this thread's y stores, device-wide, before the count
+                if (!epi_sync()) break;
+                int* list = (int*)(smem + O_LIST);
+                const int ncb = P.n_out / (2 * BM), cb = e.w / (2 * BM);
+                if (t < rows) {
+                    const int tok = P.src[e.y + t];
+                    if ((unsigned)tok < (unsigned)P.T) {
+                        __threadfence();
+                        if (atomicSub(&P.arrivals[(size_t)tok * ncb + cb], 1) == 1) {
+                            __threadfence();
+                            list[1 + atomicAdd(&list[0], 1)] = tok;
+                        }
+                    } else {
+                        set_error(P.err, MOE_DEV_ERR_BAD_ROWS);
+                    }
+                }
+                if (!epi_sync()) break;
+                const int nl = list[0];
+                __threadfence();  // the other items' y rows of these tokens
+                for (int li = t >> 6; li < nl; li += EPI_WARPS * 32 / 64) {
+                    const int tok = list[1 + li];
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = 0; k < P.K; ++k) {
+                        const int r = P.slot[(size_t)tok * P.K + k];
+                        if ((unsigned)r >= (unsigned)P.R) continue;
+                        const float wk = P.wts[(size_t)tok * P.K + k];
+                        const float4 v = __ldcg(
+                            reinterpret_cast<const float4*>(P.out + (size_t)r * P.n_out + e.w) + c4);
+                        acc.x = __fmaf_rn(wk, v.x, acc.x);
+                        acc.y = __fmaf_rn(wk, v.y, acc.y);
+                        acc.z = __fmaf_rn(wk, v.z, acc.z);
+                        acc.w = __fmaf_rn(wk, v.w, acc.w);
+                    }
+                    reinterpret_cast<float4*>(P.comb + (size_t)tok * P.n_out + e.w)[c4] = acc;
+                }
+                if (!epi_sync()) break;  // the list is read and the staging buffer free
+                if (t == 0) list[0] = 0;
+            } else {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                if (!epi_sync()) break;
+                if (warp == 0) {
+                    const uint32_t bytes = (GU ? BM : 2 * BM) * 4;
+                    for (int n = lane; n < rows; n += 32)
+                        bulk_s2g(P.out + (size_t)(e.y + n) * P.n_out + e.w,
+                                 smem_u32(st + n * STAGE_W), bytes);
+                    bulk_commit();
+                    bulk_wait_read0();
+                }
+                if (!epi_sync()) break;  // the staging buffer is free again
             }
-            if (!epi_sync()) break;  // the staging buffer is free again
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_IE + i % IR));
         }
@@ -767,14 +831,14 @@ __global__ void __launch_bounds__(THREADS, 1) mmq_fold_kernel(const Params P) {
 constexpr int kMaxDevices = 64;
 
 // Per device: the shared-memory opt-in of each instantiation, and the SM count.
-template <int WT, bool GU>
+template <int WT, bool GU, bool CMB>
 bool kernel_ready(int dev) {
     static std::mutex mu;
     static signed char state[kMaxDevices] = {};  // 0 unknown, 1 ready, -1 failed
     if (dev < 0 || dev >= kMaxDevices) return false;
     std::lock_guard<std::mutex> lock(mu);
     if (state[dev] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(mmq_fold_kernel<WT, GU>,
+        cudaError_t e = cudaFuncSetAttribute(mmq_fold_kernel<WT, GU, CMB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         state[dev] = e == cudaSuccess ? 1 : -1;
         if (e != cudaSuccess && std::getenv("MOE_DEBUG"))
@@ -792,13 +856,13 @@ int sm_count(int dev) {
     return sms[dev];
 }
 
-template <int WT, bool GU>
+template <int WT, bool GU, bool CMB>
 int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* xq,
            const uint16_t* xds, int R, int d, int f, float* out, uint8_t* ws, const WsLayout& W,
-           cudaStream_t stream) {
+           const MmqFused& F, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (!kernel_ready<WT, GU>(dev)) return MOE_ERR_UNSUPPORTED;
+    if (!kernel_ready<WT, GU, CMB>(dev)) return MOE_ERR_UNSUPPORTED;
     const RecLayout RL = rec_layout(WT, d, f);
     const MatLayout& ML = GU ? RL.gu : RL.dn;
     Params P;
@@ -828,11 +892,19 @@ int launch(const uint8_t* group_base, size_t slot_stride, int E, const int8_t* x
     P.xds = reinterpret_cast<const uint32_t*>(xds);
     P.out = out;
     P.err = (uint32_t*)(ws + W.err);
+    P.comb = F.comb;
+    P.src = F.src;
+    P.slot = F.slot;
+    P.wts = F.w;
+    P.arrivals = F.arrivals;
+    P.K = F.K;
+    P.T = F.T;
+    P.R = R;
     (void)E;
     const long long upper = ((long long)R / BN + E + 1) * P.mt_count;
     const int sms = sm_count(dev);
     const int grid = (int)(upper < sms ? upper : sms);
-    mmq_fold_kernel<WT, GU><<<grid, THREADS, SMEM, stream>>>(P);
+    mmq_fold_kernel<WT, GU, CMB><<<grid, THREADS, SMEM, stream>>>(P);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess && std::getenv("MOE_DEBUG"))
@@ -851,14 +923,17 @@ bool mmq_fold_supported(int wtype, int d, int f) {
 int launch_mmq_fold(int wtype, bool gateup, const uint8_t* group_base, size_t slot_stride,
                     const int32_t* active, const int32_t* n_active, const int32_t* offsets, int E,
                     const int8_t* xq, const uint16_t* xds, int R, int d, int f, float* out,
-                    uint8_t* ws, const WsLayout& W, cudaStream_t stream) {
+                    uint8_t* ws, const WsLayout& W, const MmqFused& F, cudaStream_t stream) {
+    if (F.hq || (F.comb && gateup)) return MOE_ERR_UNSUPPORTED;
     int rc = launch_mmq_tiles(active, n_active, offsets, E, R, fold::BN, ws, W, stream);
     if (rc != MOE_OK) return rc;
-#define MOE_FOLD(WT)                                                                              \
-    return gateup ? fold::launch<WT, true>(group_base, slot_stride, E, xq, xds, R, d, f, out, ws, \
-                                           W, stream)                                             \
-                  : fold::launch<WT, false>(group_base, slot_stride, E, xq, xds, R, d, f, out,    \
-                                            ws, W, stream)
+#define MOE_FOLD(WT)                                                                             \
+    return gateup ? fold::launch<WT, true, false>(group_base, slot_stride, E, xq, xds, R, d, f,  \
+                                                  out, ws, W, F, stream)                         \
+           : F.comb ? fold::launch<WT, false, true>(group_base, slot_stride, E, xq, xds, R, d, f, \
+                                                    out, ws, W, F, stream)                       \
+                    : fold::launch<WT, false, false>(group_base, slot_stride, E, xq, xds, R, d,  \
+                                                     f, out, ws, W, F, stream)
     if (wtype == MOE_W_Q8_0) MOE_FOLD(MOE_W_Q8_0);
     if (wtype == MOE_W_Q2_0) MOE_FOLD(MOE_W_Q2_0);
     MOE_FOLD(MOE_W_Q4_1);

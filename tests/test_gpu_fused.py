@@ -4,8 +4,11 @@ moe_grouped_mmq_gateup_q8_1 must write the same q8_1 hidden bytes as the
 gate/up product followed by the stand-alone re-quantization, and
 moe_grouped_mmq_down_combine the same y rows and the same combined output as
 the down product followed by the stand-alone combine, bit for bit: the fused
-epilogues run the same arithmetic, and the combine's fixed k order does not
-depend on which work item finishes a token last.
+epilogues run the same arithmetic on the same kernel (by default the
+per-block-scaling kernel for gate/up and the folded-scale kernel for down; with
+MOE_MMQ_PATH=blockscale the per-block-scaling kernel for both), and the
+combine's fixed k order does not depend on which work item finishes a token
+last.
 
 Both fused calls are also checked against the oracle itself: the fused layer's
 output (the combine written by moe_grouped_mmq_down_combine) within 2e-3
@@ -30,25 +33,39 @@ if not torch.cuda.is_available():
 import quantized_routed_expert_q8_gb300 as m  # noqa: E402
 
 
-def _both(layer, x, ids, w):
-    """(unfused, fused) copies of hq, hds, y and out for one input.  The unfused
-    layer runs the per-block-scaling tensor-core kernel for both projections
-    (MOE_MMQ_PATH=blockscale), the kernel the fused epilogues extend."""
+PATHS = [None, "blockscale"]
+
+
+class _path:
+    """MOE_MMQ_PATH set to path (None: unset) inside the block, restored after."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        self.old = os.environ.get("MOE_MMQ_PATH")
+        if self.path is None:
+            os.environ.pop("MOE_MMQ_PATH", None)
+        else:
+            os.environ["MOE_MMQ_PATH"] = self.path
+
+    def __exit__(self, *exc):
+        if self.old is None:
+            os.environ.pop("MOE_MMQ_PATH", None)
+        else:
+            os.environ["MOE_MMQ_PATH"] = self.old
+
+
+def _both(layer, x, ids, w, path=None):
+    """(unfused, fused) copies of hq, hds, y and out for one input, both with
+    MOE_MMQ_PATH=path (None: the default kernels)."""
     res = []
     for fused in (False, True):
         for t in (layer.hq, layer.hds, layer.y, layer.out):
             t.zero_()
-        old = os.environ.get("MOE_MMQ_PATH")
-        if not fused:
-            os.environ["MOE_MMQ_PATH"] = "blockscale"
-        try:
+        with _path(path):
             out = layer.forward(x, ids, w, fused=fused)
             torch.cuda.synchronize()
-        finally:
-            if old is None:
-                os.environ.pop("MOE_MMQ_PATH", None)
-            else:
-                os.environ["MOE_MMQ_PATH"] = old
         res.append({"hq": layer.hq.clone(), "hds": layer.hds.clone(), "y": layer.y.clone(),
                     "out": out.clone(), "err": m.moe_device_error(layer.ws)})
     return res
@@ -60,19 +77,21 @@ def _assert_same(a, b):
     assert a["err"] == b["err"]
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name", [mw.TINY.name, mw.T600.name, mw.T2048.name, mw.T2048_Q2.name,
                                   mw.T2048_Q2K.name, mw.T8192.name])
-def test_fused_equals_seven_calls(name):
+def test_fused_equals_seven_calls(name, path):
     wl = H.workload(name)
     cfg = wl.cfg
     layer = m.MoeLayer(cfg.wtype, cfg.E, cfg.d, cfg.f, cfg.K, cfg.T, H.to_dev(wl.arena),
                        wl.rec_bytes, wl.arena_stride)
-    a, b = _both(layer, H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w))
+    a, b = _both(layer, H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w), path)
     assert a["err"] == 0
     _assert_same(a, b)
     # again: the arrival counters are set afresh by every call
-    out2 = layer.forward(H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w), fused=True).clone()
-    torch.cuda.synchronize()
+    with _path(path):
+        out2 = layer.forward(H.to_dev(wl.x), H.to_dev(wl.ids), H.to_dev(wl.w), fused=True).clone()
+        torch.cuda.synchronize()
     assert torch.equal(out2, a["out"])
 
 
@@ -84,19 +103,21 @@ def _small(wtype, T, ids, seed, E=10, d=256, f=128):
     return layer, H.to_dev(x), H.to_dev(np.ascontiguousarray(ids, np.int32)), H.to_dev(w)
 
 
-def test_fused_ragged_expert_sizes():
+@pytest.mark.parametrize("path", PATHS)
+def test_fused_ragged_expert_sizes(path):
     """Experts with 1 .. 257 rows: partial 16-row tiles and 128-token items."""
     sizes = [1, 15, 16, 17, 127, 128, 129, 257]
     ids = np.concatenate([np.full(n, e + 1, np.int32) for e, n in enumerate(sizes)])
     ids = np.random.default_rng(5).permutation(ids).reshape(-1, 1)
     layer, x, idd, w = _small(mw.Q8_0, ids.shape[0], ids, 31)
-    a, b = _both(layer, x, idd, w)
+    a, b = _both(layer, x, idd, w, path)
     assert a["err"] == 0
     _assert_same(a, b)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("wtype", [mw.Q8_0, mw.Q4_1, mw.Q2_0])
-def test_fused_dropped_ids(wtype):
+def test_fused_dropped_ids(wtype, path):
     """Some of a token's ids are out of range (fewer rows to combine) and some
     tokens have none (a zero output row, whatever the buffer held)."""
     T, K, E = 300, 4, 10
@@ -105,13 +126,14 @@ def test_fused_dropped_ids(wtype):
     ids[rng.random((T, K)) < 0.2] = E + 3
     ids[::37] = -1
     layer, x, idd, w = _small(wtype, T, ids, 32, E=E)
-    a, b = _both(layer, x, idd, w)
+    a, b = _both(layer, x, idd, w, path)
     assert a["err"] & m.DEV_ERR_BAD_EXPERT_ID
     _assert_same(a, b)
     assert not b["out"][::37].any()
     layer.out.fill_(float("nan"))
-    out = layer.forward(x, idd, w, fused=True)
-    torch.cuda.synchronize()
+    with _path(path):
+        out = layer.forward(x, idd, w, fused=True)
+        torch.cuda.synchronize()
     assert torch.equal(out, b["out"])
 
 
@@ -172,8 +194,9 @@ def test_fused_layer_matches_oracle(name):
 def test_down_combine_matches_oracle(name):
     """moe_grouped_mmq_down_combine alone, on hidden rows quantized by the
     oracle: its combined output against the oracle's down product followed by
-    the oracle's combine, within 1e-5 relative L2 per token (the stage-level
-    bar of the down product; the combine adds K fp32 roundings)."""
+    the oracle's combine, within 5e-5 relative L2 per token (the stage-level
+    bar of the folded-scale down product, which the call runs by default; the
+    combine adds K fp32 roundings)."""
     wl = H.workload(name)
     cfg = wl.cfg
     T, K, d, f = cfg.T, cfg.K, cfg.d, cfg.f
@@ -200,4 +223,4 @@ def test_down_combine_matches_oracle(name):
     n = len(toks)  # the oracle's combine on the selected tokens' rows, renumbered
     ref = oracle.combine_topk(y_rows, np.arange(n * K, dtype=np.int32), wl.w[toks], n, K, d)
     err = H.rel_l2_rows(out[toks], ref)
-    assert err.max() <= 1e-5, (err.max(), toks[np.argmax(err)])
+    assert err.max() <= 5e-5, (err.max(), toks[np.argmax(err)])
