@@ -282,11 +282,14 @@ int moe_combine_topk(const float* y, int R, const int32_t* slot, const float* w,
  * item that writes a token's last row computes out[t, those columns] with
  * stage 7's arithmetic (fma chain over k ascending from 0), so out is
  * bit-identical to moe_grouped_mmq_down followed by moe_combine_topk whatever
- * the order in which items finish.  A token with no valid row gets a zero row.
+ * the order in which items finish, on the same kernel moe_grouped_mmq_down
+ * picks (folded scales by default, per-block scaling under
+ * MOE_MMQ_PATH=blockscale).  A token with no valid row gets a zero row.
  *   src [R] and slot [T*K] from stage 1; w float [T*K]; out float [T][d] out,
  *   16-byte aligned; R must equal T*K.  The workspace is the one
- *   moe_workspace_size(T, K, E, d, f) sizes.  Tensor-core kernel only, as the
- *   gate/up fusion (MOE_ERR_UNSUPPORTED otherwise); otherwise as stage 6.
+ *   moe_workspace_size(T, K, E, d, f) sizes.  Tensor-core shapes only
+ *   (MOE_ERR_UNSUPPORTED otherwise, and under MOE_MMQ_PATH=simt); otherwise as
+ *   stage 6.
  */
 int moe_grouped_mmq_down_combine(int wtype, const uint8_t* group_base, size_t slot_stride,
                                  const int32_t* active, const int32_t* n_active,
