@@ -250,7 +250,7 @@ PROFILED_TRAFFIC = {
         "code_sha256_16": "a3765f4cd7855d9f", "bytes": 609651200 + 254658304},
     ("mmq_down", "T8192_d2048_f768_E512_K10_q8_0_zipf"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/mmq_fold.cu",
-        "code_sha256_16": "92e5b88589c25a62", "bytes": 275763200 + 667117824},
+        "code_sha256_16": "3426d9a626cde64a", "bytes": 275820544 + 666888704},
     ("quantize_scatter", "T32768_d2048_f768_E512_K10_q4_1"): {
         "source": "quantized_routed_expert_q8_gb300/csrc/quantize.cu",
         "code_sha256_16": "217e4c4ac0275670", "bytes": 270006272 + 694668800},
