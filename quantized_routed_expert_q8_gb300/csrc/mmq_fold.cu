@@ -41,7 +41,10 @@
 //     issuer's barrier probes and commits overlap the other's MMAs;
 //   epilogue (warps 0-7): once per item, the accumulator -> a shared-memory
 //     staging buffer (the accumulator is released as soon as it is copied),
-//     SiLU(g)*u for stage 4, then one bulk copy per output row.
+//     SiLU(g)*u for stage 4, then one bulk copy per output row; the CMB
+//     instantiation (stage 6 with the top-k combine) stores the rows with
+//     generic stores instead, counts each row's token down and combines the
+//     tokens whose last row the item wrote.
 // Every wait is bounded: on timeout the kernel sets MOE_DEV_ERR_TIMEOUT,
 // drains what it started and exits.
 #include <cstdio>
