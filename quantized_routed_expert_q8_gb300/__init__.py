@@ -347,11 +347,19 @@ class MoeLayer:
         self.ws = torch.zeros((ws_bytes + 255) // 256 * 256, dtype=torch.uint8, device=device)
         moe_workspace_init(self.ws)
 
+    def _out_writable(self, stream):
+        """Order the stream's next write of the output buffer after the copies back
+        of a forward_host call that was not waited for."""
+        ev = getattr(self, "_out_free", None)
+        if ev is not None:
+            (stream if stream is not None else torch.cuda.current_stream()).wait_event(ev)
+
     def forward(self, x, ids, w, stream=None, fused=False):
         """x f32 [T, d], ids int32 [T, K], w f32 [T, K] on the GPU -> out [T, d]
         (a view of the layer's output buffer).  fused=True runs stages 4+5 and
         6+7 as the two fused calls (same bytes; tensor-core shapes only)."""
         T = x.shape[0]
+        self._out_writable(stream)
         assert T <= self.T_max and ids.shape == (T, self.K) and w.shape == (T, self.K)
         K, E, d, f = self.K, self.E, self.d, self.f
         R = T * K
@@ -503,6 +511,7 @@ class MoeLayer:
             setattr(b, name, t.data_ptr())
         b.ws_bytes = self.ws.numel()
         cs = stream if stream is not None else torch.cuda.current_stream(dev)
+        self._out_writable(cs)
         moe_layer_forward_streamed(self.wtype, x, ids, w, self.out, host_arena, self.rec_bytes,
                                    self.arena_stride, self.slot_stride, ring_groups, b, self.E,
                                    self.f, cs, self.copy_stream)

@@ -106,13 +106,18 @@ def test_forward_host_back_to_back(name):
     assert not np.array_equal(refs[0], refs[1]) and not np.array_equal(refs[0], refs[2])
     host = [tuple(torch.from_numpy(a).pin_memory() for a in inp) for inp in inputs]
     outs = [torch.full((cfg.T, cfg.d), float("nan")).pin_memory() for _ in inputs]
+    dev_in = [tuple(H.to_dev(a) for a in inp) for inp in inputs]
     for _ in range(2):
         for o in outs:
             o.fill_(float("nan"))
         events = [layer.forward_host(hx, hids, hw, o, wait=False)
                   for (hx, hids, hw), o in zip(host, outs)]
+        # a device-input call queued at once rewrites the output buffer only
+        # after the last copy back has read it
+        last = layer.forward(*dev_in[0])
         for ev, o, ref in zip(events, outs, refs):
             ev.synchronize()
             assert np.array_equal(o.numpy(), ref)
+        assert np.array_equal(last.cpu().numpy(), refs[0])
         torch.cuda.current_stream().synchronize()
         assert m.moe_device_error(layer.ws) == 0
