@@ -257,6 +257,14 @@ int moe_grouped_mmq_gateup_q8_1(int wtype, const uint8_t* group_base, size_t slo
  * stage 4), fp32.
  *   hq, hds from stage 5 (D2S6 for MOE_W_Q2_K); y float [R][d] out.  Alignment
  *   and shapes as stage 4.
+ * Q8_0, Q4_1 and Q2_0 shapes that fit the tensor cores run by default on the
+ * folded-scale kernel: each dequantized value d*q is split exactly into two
+ * binary16 terms and the whole reduction accumulates in fp32 on the tensor
+ * cores, so y differs from the definition's per-block order of roundings by at
+ * most a few fp32 units of the sum of |w*x| (the accumulation count times
+ * 2^-23, the smallest cross term dropped at 2^-22).  MOE_MMQ_PATH=blockscale
+ * selects the per-block-scaling kernel, whose y equals the definition's bit
+ * for bit.
  */
 int moe_grouped_mmq_down(int wtype, const uint8_t* group_base, size_t slot_stride,
                          const int32_t* active, const int32_t* n_active, const int32_t* offsets,
